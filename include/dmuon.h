@@ -1,0 +1,226 @@
+/*
+ * dmuon.h -- C ABI of the GB300 batched Gram-space Newton-Schulz Muon step.
+ *
+ * Subject: "DMuon: Efficient Distributed Muon Training with Near-Adam
+ * Overhead" (arXiv 2606.27153), gist.science technical summary (pt/fr),
+ * section 2.2 "Gram Newton-Schulz iteration": the owner of a weight matrix
+ * runs Newton-Schulz on its momentum-aggregated gradient in the m x m Gram
+ * space G = X X^T (m < n), forms G SYRK-style (lower triangle only), and
+ * batches matrices of like shape so small ones do not leave the GPU idle.
+ * This library is that per-owner compute on one GPU: no ranks, no
+ * collectives.
+ *
+ * One optimizer step, per matrix W (rows x cols) with gradient and momentum
+ * of the same shape and dtype:
+ *   M' = beta*M + grad;  U = grad + beta*M'       (Nesterov; option: U = M')
+ *   X  = U (rows <= cols) or U^T (rows > cols):    m x n, m = min, n = max
+ *   X0 = X / (||X||_F + eps)
+ *   T Newton-Schulz steps with the quintic (a, b, c):
+ *     Gram route:   R = X0 X0^T; per step P = aI + bR + cR^2, Q <- P Q,
+ *                   R <- P R P; result Q X0
+ *     direct route: per step A = X X^T, B = bA + cA^2, X <- aX + B X
+ *   W' = (1 - lr*wd) W - lr*s*O,  O = result in W's orientation,
+ *   s = sqrt(max(1, rows/cols)) (option: 0.2*sqrt(max(rows, cols))).
+ * The pages fix neither coefficients, eps, momentum form nor update scale;
+ * the defaults are the published Muon ones: (3.4445, -4.7750, 2.0315),
+ * T = 5, eps = 1e-7, Nesterov, aspect scale.
+ *
+ * Conventions for every entry point:
+ *  - Pointer arrays are HOST arrays of `count` DEVICE pointers, in the order
+ *    of the shapes given to dmuon_plan.  Each tensor is row-major,
+ *    contiguous, rows x cols elements of the shape's dtype, and starts on a
+ *    16-byte boundary (else DMUON_ERR_ALIGN).
+ *  - The caller owns params, grads, momenta and the workspace.  The library
+ *    owns only host-side plan data.  params and momenta are updated in place;
+ *    grads are read only.
+ *  - dmuon_step is asynchronous on `stream` (a cudaStream_t passed as void*,
+ *    NULL = legacy default stream).  It allocates nothing and never
+ *    synchronises the host, except that a change of the pointer set since the
+ *    previous step uploads the new pointer table with one pageable copy.
+ *  - Errors are negative status codes; dmuon_last_error() gives the message
+ *    of the calling thread's last failure.  A handle must not be used on two
+ *    streams at once.
+ *  - Every device-side wait inside the kernels is bounded; on time-out the
+ *    kernel records DMUON_ERR_DEVICE_TIMEOUT in the workspace status word and
+ *    returns.  dmuon_device_status() reads (and clears) it.
+ */
+#ifndef DMUON_H
+#define DMUON_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* storage dtypes of W, grad and momentum */
+#define DMUON_BF16 0
+#define DMUON_FP32 1
+
+/* precision modes */
+#define DMUON_PREC_BF16 0 /* tcgen05 tensor cores, bf16 operands, fp32 accumulation (default) */
+#define DMUON_PREC_FP32 1 /* fp32 FFMA (SIMT) for every product: validation mode */
+
+/* route rules (which Newton-Schulz form a bucket runs) */
+#define DMUON_ROUTE_AUTO 0   /* Gram when n >= 2m or m <= small_m, else direct */
+#define DMUON_ROUTE_GRAM 1   /* Gram space for every bucket */
+#define DMUON_ROUTE_DIRECT 2 /* direct m x n iteration for every bucket */
+
+/* per-bucket route and m x m engine reported by dmuon_plan_bucket */
+#define DMUON_BUCKET_GRAM 1
+#define DMUON_BUCKET_DIRECT 2
+#define DMUON_ENGINE_TC_BF16 0 /* tensor cores, bf16 operands */
+#define DMUON_ENGINE_SIMT_FP32 1 /* fp32 FFMA */
+
+/* update-scale rules */
+#define DMUON_SCALE_ASPECT 0 /* s = sqrt(max(1, rows/cols)) */
+#define DMUON_SCALE_RMS 1    /* s = 0.2*sqrt(max(rows, cols)) */
+
+/* status codes */
+#define DMUON_OK 0
+#define DMUON_ERR_INVALID_ARG -1
+#define DMUON_ERR_ALIGN -2
+#define DMUON_ERR_NO_WORKSPACE -3
+#define DMUON_ERR_UNSUPPORTED_DTYPE -4
+#define DMUON_ERR_CUDA -5
+#define DMUON_ERR_DEVICE_TIMEOUT -6
+#define DMUON_ERR_UNSUPPORTED_DEVICE -7
+#define DMUON_ERR_WORKSPACE_TOO_SMALL -8
+
+/* limits checked by dmuon_plan */
+#define DMUON_MAX_DIM (1 << 20)      /* rows, cols <= 2^20 */
+#define DMUON_MAX_ELEMS (1LL << 31)  /* rows*cols < 2^31 */
+#define DMUON_MAX_NS_STEPS 16
+
+typedef struct dmuon_plan_s* dmuon_handle_t;
+
+typedef struct {
+    int64_t rows;     /* >= 1 */
+    int64_t cols;     /* >= 1 */
+    int32_t dtype;    /* DMUON_BF16 | DMUON_FP32 */
+    int32_t reserved; /* must be 0 */
+} dmuon_shape_t;
+
+/* Zero-initialised options give the defaults noted on each field. */
+typedef struct {
+    int32_t precision;      /* DMUON_PREC_*; default DMUON_PREC_BF16 */
+    int32_t route;          /* DMUON_ROUTE_*; default AUTO */
+    float ns_a, ns_b, ns_c; /* quintic coefficients; all 0 => (3.4445, -4.7750, 2.0315) */
+    float eps;              /* normalisation epsilon; 0 => 1e-7 */
+    int32_t scale_rule;     /* DMUON_SCALE_*; default ASPECT */
+    int32_t no_nesterov;    /* 0 => Nesterov U = grad + beta*M'; 1 => U = M' */
+    int32_t small_m;        /* AUTO route and BF16 mode: Gram buckets with m <= small_m run
+                               their m x m products in fp32 FFMA; 0 => 256; < 0 => none */
+    int32_t reserved;
+    uint64_t workspace_budget; /* bytes for one wave of buckets; 0 => everything in one wave */
+} dmuon_options_t;
+
+typedef struct {
+    int32_t dtype;     /* DMUON_BF16 | DMUON_FP32 */
+    int32_t route;     /* DMUON_BUCKET_GRAM | DMUON_BUCKET_DIRECT */
+    int32_t mm_engine; /* DMUON_ENGINE_* used for the m x m products */
+    int32_t reserved;
+    int64_t m, n;      /* canonical short and long side */
+    int64_t count;     /* matrices in the bucket */
+    int64_t per_matrix_bytes; /* workspace bytes one matrix of the bucket needs in a wave */
+} dmuon_bucket_info_t;
+
+/* ---- planning (host only: no CUDA call, works without a GPU) ---------- */
+
+/* Shape-bucketing planner.  Each shape is canonicalised to (m, n, transposed)
+ * with m = min(rows, cols), n = max(rows, cols), transposed = rows > cols
+ * (tall matrices are packed transposed).  Buckets are keyed (dtype, m, n),
+ * ordered by that key ascending; matrices keep their input order inside a
+ * bucket.  Buckets are then packed, in bucket order, into waves whose
+ * workspace fits options->workspace_budget, splitting a bucket where needed.
+ * Returns NULL on error (message in dmuon_last_error): count < 1, a NULL
+ * pointer, a dimension outside [1, DMUON_MAX_DIM], rows*cols >=
+ * DMUON_MAX_ELEMS, an unknown dtype, a non-zero reserved field, bad options,
+ * or a budget smaller than one matrix. */
+dmuon_handle_t dmuon_plan(const dmuon_shape_t* shapes, int64_t count);
+dmuon_handle_t dmuon_plan_ex(const dmuon_shape_t* shapes, int64_t count,
+                             const dmuon_options_t* options);
+void dmuon_destroy(dmuon_handle_t h); /* NULL is a no-op */
+
+int64_t dmuon_plan_num_buckets(dmuon_handle_t h);
+int dmuon_plan_bucket(dmuon_handle_t h, int64_t bucket, dmuon_bucket_info_t* out);
+/* out receives `count` input indices, in bucket order */
+int dmuon_plan_bucket_members(dmuon_handle_t h, int64_t bucket, int64_t* out);
+int64_t dmuon_plan_num_waves(dmuon_handle_t h);
+int64_t dmuon_plan_wave_num_pieces(dmuon_handle_t h, int64_t wave);
+/* piece = matrices [start, start+count) of bucket `bucket` (bucket order) */
+int dmuon_plan_wave_piece(dmuon_handle_t h, int64_t wave, int64_t piece,
+                          int64_t* bucket, int64_t* start, int64_t* count);
+/* Algorithmic FLOPs of one step with `ns_steps` iterations: 2 per
+ * multiply-add, symmetric outputs counted once (SYRK and the m x m products
+ * at half).  Gram bucket: (3 m^2 n + (4T-3) m^3) per matrix; direct bucket:
+ * T (3 m^2 n + m^3).  Written to out[0]; out[1] gets the part run on tensor
+ * cores.  Returns DMUON_OK. */
+int dmuon_plan_flops(dmuon_handle_t h, int32_t ns_steps, double* out);
+
+/* ---- workspace --------------------------------------------------------- */
+
+/* Device bytes the caller must provide (256-byte aligned). */
+size_t dmuon_workspace_bytes(dmuon_handle_t h);
+/* Binds caller-owned device memory (e.g. a torch uint8 tensor) of at least
+ * dmuon_workspace_bytes(h) bytes, 256-byte aligned, on the current device.
+ * Builds the TMA tensor maps and launch tables and copies them into the
+ * workspace (synchronous).  Needs an sm_103 GPU: DMUON_ERR_UNSUPPORTED_DEVICE
+ * otherwise. */
+int dmuon_bind_workspace(dmuon_handle_t h, void* dev_ptr, size_t bytes);
+
+/* ---- the step ---------------------------------------------------------- */
+
+/* One Muon step over every planned matrix (formula in the file header).
+ * params[i], grads[i], momenta[i]: device pointers of shape i.  lr, wd >= 0,
+ * 0 <= beta < 1 (finite), 1 <= ns_steps <= DMUON_MAX_NS_STEPS.  Errors:
+ * INVALID_ARG (NULL arrays or pointers, bad scalars), ALIGN,
+ * NO_WORKSPACE, CUDA (launch failure). */
+int dmuon_step(dmuon_handle_t h, void* const* params, const void* const* grads,
+               void* const* momenta, float lr, float beta, float wd,
+               int32_t ns_steps, void* stream);
+
+/* Synchronises `stream`, returns the device status word (DMUON_OK or
+ * DMUON_ERR_DEVICE_TIMEOUT) and clears it. */
+int dmuon_device_status(dmuon_handle_t h, void* stream);
+
+/* ---- measurement ------------------------------------------------------- */
+
+#define DMUON_TIMER_MOMENTUM 0 /* momentum + pack + sum of squares */
+#define DMUON_TIMER_NORM 1     /* per-matrix 1/(||X||+eps) */
+#define DMUON_TIMER_SYRK 2     /* first product of every wave: Gram / first A = X X^T */
+#define DMUON_TIMER_NS 3       /* the Newton-Schulz polynomial products */
+#define DMUON_TIMER_FINAL 4    /* final product fused with the update */
+#define DMUON_TIMER_TC 5       /* every tcgen05 GEMM launch (sum) */
+#define DMUON_TIMER_SIMT 6     /* every fp32 FFMA GEMM launch (sum) */
+#define DMUON_TIMER_COUNT 7
+
+/* enable != 0 records a CUDA event pair around every launch of later steps
+ * (on the step's stream).  Resets the accumulated times. */
+int dmuon_set_timing(dmuon_handle_t h, int32_t enable);
+/* Synchronises the recorded events and writes, per DMUON_TIMER_* slot, the
+ * accumulated milliseconds to ms[slot] and the number of launches to
+ * launches[slot] (either may be NULL).  n = number of slots to write. */
+int dmuon_get_timing(dmuon_handle_t h, double* ms, int64_t* launches, int32_t n);
+
+/* ---- errors ------------------------------------------------------------ */
+
+const char* dmuon_last_error(void);       /* thread-local, never NULL */
+const char* dmuon_status_string(int status);
+
+/* ---- inspection (tests) ------------------------------------------------ */
+
+#define DMUON_BUF_X 0  /* packed u (and direct-route iterate 0) */
+#define DMUON_BUF_RF 1 /* Gram route: fp32 R after the last update; direct: fp32 A */
+
+/* Byte offset into the bound workspace, leading dimension (elements) and
+ * batch stride (elements) of buffer `which` of piece (wave, piece). */
+int dmuon_debug_buffer(dmuon_handle_t h, int64_t wave, int64_t piece, int32_t which,
+                       uint64_t* offset, int64_t* ld, int64_t* batch_stride);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DMUON_H */
