@@ -1,0 +1,347 @@
+#!/usr/bin/env python3
+"""Benchmark of one batched Muon optimizer step on a GB300.
+
+Workload (default): the Llama-3-8B-shaped set, 32 layers x {q 4096x4096,
+k 1024x4096, v 1024x4096, o 4096x4096, gate 14336x4096, up 14336x4096,
+down 4096x14336} = 224 bf16 matrices, gradients N(0,1)*1e-3 with 1 % of the
+entries x100, zero momentum, 5 Newton-Schulz steps, lr 0.02, beta 0.95,
+wd 0.01.  The step is the whole hot path: momentum + pack + norms, the Gram
+products, the Newton-Schulz polynomial products and the final product fused
+with the update.  Inputs (42 GB) are resident in HBM and larger than L2.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the fp64 CPU
+oracle instead, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["dmuon", "reference"], default="dmuon")
+    ap.add_argument("--config", default="c3", help="workload: c1..c5 (c3 is the measured one)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--budget-gb", type=float, default=0.0, help="workspace budget per wave (0 = one wave)")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples every 200 ms during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_id):
+        self.device_id = device_id
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if self.device_id is not None:
+            cmd += ["-i", str(self.device_id)]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        with open(self.path) as f:
+            for line in f:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) < 9:
+                    continue
+                try:
+                    sm.append(float(p[1]))
+                    smax.append(float(p[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, p[5:9]):
+                    if val.lower().startswith("active"):
+                        reasons.add(name)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+
+def oracle_flops(m, n, T=5):
+    """Multiply-add flops of the oracle's direct Newton-Schulz (full products)."""
+    return T * (4.0 * m * m * n + 2.0 * m ** 3)
+
+
+def oracle_sample(cfg, index):
+    """Time the fp64 oracle on matrix ``index`` of ``cfg`` (CPU inputs, same recipe)."""
+    import numpy as np
+
+    import oracle
+    import workloads
+    w, g, m = workloads.make_matrix(cfg, index, "cpu")
+    args = (w.double().numpy(), g.double().numpy(), m.double().numpy())
+    f32 = lambda x: float(np.float32(x))  # noqa: E731
+    t0 = time.perf_counter()
+    oracle.muon_step(*args, lr=f32(cfg.lr), beta=f32(cfg.beta), wd=f32(cfg.wd), ns_steps=cfg.ns_steps,
+                     dtype=cfg.dtype)
+    return time.perf_counter() - t0
+
+
+def cpu_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [x.get("num_threads") for x in threadpool_info() if x.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:  # noqa: BLE001
+        pass
+    return os.cpu_count()
+
+
+def cpu_baseline(cfg, repeats=1):
+    """Oracle matrices/s for the whole set, extrapolated from one sampled matrix by flop count."""
+    idx = min(range(len(cfg.shapes)), key=lambda i: cfg.shapes[i][0] * cfg.shapes[i][1])
+    r, c = cfg.shapes[idx]
+    t = min(oracle_sample(cfg, idx) for _ in range(repeats))
+    m, n = min(r, c), max(r, c)
+    total = sum(oracle_flops(min(a, b), max(a, b), cfg.ns_steps) for a, b in cfg.shapes)
+    t_set = t * total / oracle_flops(m, n, cfg.ns_steps)
+    return {"value": len(cfg.shapes) / t_set, "unit": "matrices/s", "cores": cpu_threads(), "kind": "oracle",
+            "sample": f"one {r}x{c} matrix (index {idx}) of the set, fp64 direct Newton-Schulz, {t:.2f} s; "
+                      f"set time extrapolated by the oracle's flop count ({t_set:.1f} s per step)"}
+
+
+# ---------------------------------------------------------------- distributed
+
+
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- arms
+
+
+def run_reference(args, cfg, world, rank):
+    """The fp64 CPU oracle as the reference arm (rank 0 only)."""
+    if rank != 0:
+        return
+    for _ in range(args.warmup):
+        cpu_baseline(cfg)
+    vals = [cpu_baseline(cfg) for _ in range(args.steps)]
+    v = statistics.median(x["value"] for x in vals)
+    base = dict(vals[0])
+    base["value"] = v
+    print(json.dumps({
+        "impl": "reference", "metric": "Muon optimizer-step matrices/s", "value": v, "unit": "matrices/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * len(cfg.shapes) / v,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workloads_name(cfg), "matrices": len(cfg.shapes), "ns_steps": cfg.ns_steps},
+        "cpu_baseline": base,
+        "e2e": {"value": v, "unit": "matrices/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def workloads_name(cfg):
+    return f"{cfg.name}: {cfg.title}"
+
+
+def run_dmuon(args, cfg, world, rank, local):
+    import torch
+
+    import workloads
+    from matrix_orthogonalising_optimizer_gb300 import Muon, _lib
+
+    _lib.load(build_if_missing=True)
+    dt = 0 if cfg.dtype == "bf16" else 1
+    budget = int(args.budget_gb * (1 << 30))
+    muon = Muon([(r, c, dt) for r, c in cfg.shapes], precision=cfg.precision, workspace_budget=budget).bind()
+    ws, gs, ms = workloads.make_set(cfg, "cuda")
+    torch.cuda.synchronize()
+    lr, beta, wd, T = cfg.lr, cfg.beta, cfg.wd, cfg.ns_steps
+    stream = torch.cuda.current_stream()
+
+    for _ in range(max(args.warmup, 0)):
+        muon.step(ws, gs, ms, lr, beta, wd, T, stream)
+    torch.cuda.synchronize()
+    if muon.device_status(stream) != 0:
+        raise RuntimeError("device status set during warm-up")
+
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    uuid = getattr(props, "uuid", None)
+    sampler = ClockSampler(f"GPU-{uuid}" if uuid is not None else local)
+    sampler.start()
+    time.sleep(0.3)
+    muon.set_timing(True)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        muon.step(ws, gs, ms, lr, beta, wd, T, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    ms_step = e0.elapsed_time(e1) / args.steps
+    timing = muon.timing()
+    muon.set_timing(False)
+    if muon.device_status(stream) != 0:
+        raise RuntimeError("device status set during the timed steps")
+    ms_step = max_over_ranks(ms_step, world)
+
+    n_mat = len(cfg.shapes)
+    value = world * n_mat / (ms_step / 1000.0)
+    flops_total, flops_tc = muon.flops(T)
+    peaks, src = load_peaks()
+    peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    tc_ms = timing["tc"][0] / args.steps
+    achieved = flops_tc / (tc_ms / 1000.0) / 1e12 if tc_ms > 0 else 0.0
+    launches = sum(timing[k][1] for k in ("momentum", "norm", "tc", "simt"))
+    stages = {k: round(v[0] / args.steps, 4) for k, v in timing.items()}
+    launches_per_step = {k: v[1] // args.steps for k, v in timing.items()}
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(muon, cfg, ws, gs, ms, args.e2e_steps, stream, world)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(cfg)
+
+    if rank == 0:
+        line = {
+            "metric": "Muon optimizer-step matrices/s", "value": value, "unit": "matrices/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if cfg.precision == "bf16" else "fp32",
+            "data": "synthetic",
+            "config": {"workload": workloads_name(cfg), "matrices": n_mat, "ns_steps": T,
+                       "elements": workloads.total_elements(cfg), "lr": lr, "beta": beta, "wd": wd,
+                       "l2": "inputs larger than L2 (resident in HBM)",
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "traffic": None,
+                         "kernel": "gemm_tc_kernel (all tcgen05 GEMM launches of a step)",
+                         "peak_source": f"bf16_tflops_sustained of {src} peaks"},
+            "gemm_algorithmic_tflop_per_step": flops_tc / 1e12,
+            "step_tflops": flops_total / (ms_step / 1000.0) / 1e12,
+            "step_frac_of_peak": flops_total / (ms_step / 1000.0) / 1e12 / peak,
+            "stages_ms_per_step": stages, "launches_per_step": launches_per_step,
+            "gpu_launches": int(launches), "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def measure_e2e(muon, cfg, ws, gs, ms, steps, stream, world):
+    """Same metric through the public API with host buffers: every step copies the
+    gradients host->device from pinned memory and reads the updated parameters back."""
+    import torch
+    host_g = [g.cpu().pin_memory() for g in gs]
+    host_w = [torch.empty(w.shape, dtype=w.dtype, pin_memory=True) for w in ws]
+    h2d = sum(g.numel() * g.element_size() for g in gs)
+    d2h = sum(w.numel() * w.element_size() for w in ws)
+    lr, beta, wd, T = cfg.lr, cfg.beta, cfg.wd, cfg.ns_steps
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        for d, h in zip(gs, host_g):
+            d.copy_(h, non_blocking=True)
+        muon.step(ws, gs, ms, lr, beta, wd, T, stream)
+        for h, d in zip(host_w, ws):
+            h.copy_(d, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms_step = max_over_ranks(e0.elapsed_time(e1) / steps, world)
+    return {"value": world * len(cfg.shapes) / (ms_step / 1000.0), "unit": "matrices/s",
+            "ms_per_step": ms_step, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def main():
+    args = parse_args()
+    import workloads
+    cfg = workloads.get(args.config)
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        run_reference(args, cfg, int(os.environ.get("WORLD_SIZE", "1")), rank)
+        return
+    world, rank, local = dist_setup(args)
+    run_dmuon(args, cfg, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

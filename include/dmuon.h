@@ -63,7 +63,7 @@ extern "C" {
 #define DMUON_PREC_FP32 1 /* fp32 FFMA (SIMT) for every product: validation mode */
 
 /* route rules (which Newton-Schulz form a bucket runs) */
-#define DMUON_ROUTE_AUTO 0   /* Gram when n >= 2m or m <= small_m, else direct */
+#define DMUON_ROUTE_AUTO 0   /* Gram when n >= 3m or m <= small_m, else direct */
 #define DMUON_ROUTE_GRAM 1   /* Gram space for every bucket */
 #define DMUON_ROUTE_DIRECT 2 /* direct m x n iteration for every bucket */
 

@@ -1,0 +1,169 @@
+"""GB300 batched Gram-space Newton-Schulz Muon step.
+
+A thin binding over the C ABI of ``include/dmuon.h`` (``libdmuon.so``): it
+only marshals arguments.  Every step of the computation runs in the CUDA
+kernels; PyTorch supplies device memory (the workspace) and streams.  There
+is no CPU fallback: without the built library every call raises.
+
+Subject: "DMuon: Efficient Distributed Muon Training with Near-Adam Overhead"
+(arXiv 2606.27153), the per-owner Gram Newton-Schulz engine of its section
+2.2 (gist.science technical summary), on one GPU.
+"""
+from __future__ import annotations
+
+import ctypes
+
+from . import _lib
+from ._lib import (  # noqa: F401
+    BF16, FP32, PREC_BF16, PREC_FP32, ROUTE_AUTO, ROUTE_GRAM, ROUTE_DIRECT, BUCKET_GRAM, BUCKET_DIRECT,
+    ENGINE_TC_BF16, ENGINE_SIMT_FP32, SCALE_ASPECT, SCALE_RMS, TIMER_NAMES, DmuonError,
+)
+
+__all__ = ["Muon", "dmuon_plan", "dmuon_step", "load"]
+
+_DTYPES = {"bf16": BF16, "fp32": FP32}
+_PREC = {"bf16": PREC_BF16, "fp32": PREC_FP32}
+_ROUTES = {"auto": ROUTE_AUTO, "gram": ROUTE_GRAM, "direct": ROUTE_DIRECT}
+_SCALES = {"aspect": SCALE_ASPECT, "rms": SCALE_RMS}
+
+
+def load():
+    return _lib.load()
+
+
+def _stream_handle(stream):
+    if stream is None:
+        import torch
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def dmuon_plan(shapes, dtype="bf16", precision="bf16", route="auto", coeffs=None, eps=0.0,
+               scale_rule="aspect", nesterov=True, small_m=0, workspace_budget=0):
+    """dmuon_plan_ex: shapes is a list of (rows, cols) or (rows, cols, dtype)."""
+    lib = _lib.load()
+    arr = (_lib.Shape * len(shapes))()
+    for i, s in enumerate(shapes):
+        dt = s[2] if len(s) > 2 else dtype
+        arr[i].rows, arr[i].cols = int(s[0]), int(s[1])
+        arr[i].dtype = _DTYPES[dt] if isinstance(dt, str) else int(dt)
+        arr[i].reserved = 0
+    opt = _lib.Options()
+    opt.precision = _PREC[precision]
+    opt.route = _ROUTES[route]
+    if coeffs is not None:
+        opt.ns_a, opt.ns_b, opt.ns_c = coeffs
+    opt.eps = eps
+    opt.scale_rule = _SCALES[scale_rule]
+    opt.no_nesterov = 0 if nesterov else 1
+    opt.small_m = small_m
+    opt.workspace_budget = workspace_budget
+    h = lib.dmuon_plan_ex(arr, len(shapes), ctypes.byref(opt))
+    if not h:
+        raise DmuonError(_lib.ERR_INVALID_ARG, "dmuon_plan_ex")
+    return h
+
+
+def dmuon_step(h, params, grads, momenta, lr, beta, wd, ns_steps=5, stream=None):
+    """dmuon_step over lists of device tensors (or raw device pointers)."""
+    lib = _lib.load()
+    n = len(params)
+
+    def ptrs(xs):
+        a = (ctypes.c_void_p * n)()
+        for i, x in enumerate(xs):
+            a[i] = x if isinstance(x, int) else x.data_ptr()
+        return a
+
+    st = lib.dmuon_step(h, ptrs(params), ptrs(grads), ptrs(momenta), lr, beta, wd, ns_steps,
+                        _stream_handle(stream))
+    _lib.check(st, "dmuon_step")
+
+
+class Muon:
+    """One plan bound to a workspace: ``Muon(shapes).step(params, grads, moms, lr, beta, wd)``.
+
+    ``shapes``: list of (rows, cols[, dtype]).  The workspace is a torch uint8
+    tensor on the current CUDA device unless one is passed to ``bind``.
+    """
+
+    def __init__(self, shapes, **plan_kw):
+        self.lib = _lib.load()
+        self.shapes = [tuple(s) for s in shapes]
+        self.handle = dmuon_plan(shapes, **plan_kw)
+        self.workspace = None
+
+    def __del__(self):
+        h = getattr(self, "handle", None)
+        if h:
+            self.lib.dmuon_destroy(h)
+            self.handle = None
+
+    # ---- plan queries
+    def workspace_bytes(self) -> int:
+        return int(self.lib.dmuon_workspace_bytes(self.handle))
+
+    def buckets(self):
+        out = []
+        for b in range(self.lib.dmuon_plan_num_buckets(self.handle)):
+            info = _lib.BucketInfo()
+            _lib.check(self.lib.dmuon_plan_bucket(self.handle, b, ctypes.byref(info)), "dmuon_plan_bucket")
+            mem = (ctypes.c_int64 * info.count)()
+            _lib.check(self.lib.dmuon_plan_bucket_members(self.handle, b, mem), "dmuon_plan_bucket_members")
+            out.append({"dtype": info.dtype, "m": info.m, "n": info.n, "route": info.route,
+                        "engine": info.mm_engine, "per_matrix_bytes": info.per_matrix_bytes,
+                        "members": list(mem)})
+        return out
+
+    def waves(self):
+        out = []
+        for w in range(self.lib.dmuon_plan_num_waves(self.handle)):
+            pieces = []
+            for p in range(self.lib.dmuon_plan_wave_num_pieces(self.handle, w)):
+                b, s, c = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+                _lib.check(self.lib.dmuon_plan_wave_piece(self.handle, w, p, ctypes.byref(b), ctypes.byref(s),
+                                                          ctypes.byref(c)), "dmuon_plan_wave_piece")
+                pieces.append((b.value, s.value, c.value))
+            out.append(pieces)
+        return out
+
+    def flops(self, ns_steps=5):
+        out = (ctypes.c_double * 2)()
+        _lib.check(self.lib.dmuon_plan_flops(self.handle, ns_steps, out), "dmuon_plan_flops")
+        return out[0], out[1]
+
+    # ---- device
+    def bind(self, workspace=None):
+        import torch
+        nbytes = self.workspace_bytes()
+        if workspace is None:
+            workspace = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+        self.workspace = workspace
+        _lib.check(self.lib.dmuon_bind_workspace(self.handle, ctypes.c_void_p(workspace.data_ptr()),
+                                                 workspace.numel() * workspace.element_size()),
+                   "dmuon_bind_workspace")
+        return self
+
+    def step(self, params, grads, momenta, lr, beta, wd, ns_steps=5, stream=None):
+        dmuon_step(self.handle, params, grads, momenta, lr, beta, wd, ns_steps, stream)
+
+    def device_status(self, stream=None) -> int:
+        return int(self.lib.dmuon_device_status(self.handle, _stream_handle(stream)))
+
+    def set_timing(self, enable: bool):
+        _lib.check(self.lib.dmuon_set_timing(self.handle, 1 if enable else 0), "dmuon_set_timing")
+
+    def timing(self):
+        n = len(TIMER_NAMES)
+        ms = (ctypes.c_double * n)()
+        cnt = (ctypes.c_int64 * n)()
+        _lib.check(self.lib.dmuon_get_timing(self.handle, ms, cnt, n), "dmuon_get_timing")
+        return {k: (ms[i], cnt[i]) for i, k in enumerate(TIMER_NAMES)}
+
+    def debug_buffer(self, wave, piece, which):
+        off, ld, bs = ctypes.c_uint64(), ctypes.c_int64(), ctypes.c_int64()
+        _lib.check(self.lib.dmuon_debug_buffer(self.handle, wave, piece, which, ctypes.byref(off), ctypes.byref(ld),
+                                               ctypes.byref(bs)), "dmuon_debug_buffer")
+        return off.value, ld.value, bs.value

@@ -1,0 +1,487 @@
+// Persistent batched GEMM on the 5th-generation tensor cores (sm_103a).
+//
+// The products of the Gram-space Newton-Schulz step (DMuon technical summary
+// on gist.science, section 2.2): the Gram matrix X X^T formed SYRK-style
+// (lower-triangle tiles only, mirrored in the epilogue), the m x m polynomial
+// products -- all symmetric, so the same triangular schedule applies -- and
+// the final Q X0 product fused with the Muon update.  Matrices of one shape
+// bucket are batched as the third TMA coordinate, and one launch covers every
+// group (bucket x product) of a phase, so small matrices share the machine
+// (section 2.2 "batching").
+//
+// Layout of one CTA (one per SM, persistent over a static round-robin tile
+// schedule):
+//   warp 0      one thread issues TMA loads into a 4-stage shared-memory ring
+//   warp 1      allocates 512 TMEM columns; one thread issues tcgen05.mma
+//               (kind::f16, bf16 operands, fp32 accumulation) into one of two
+//               128 x 256 fp32 accumulators
+//   warps 2..5  epilogue: tcgen05.ld the accumulator (row per thread), apply
+//               the fused epilogue, store; releases the accumulator so the
+//               next tile's MMAs overlap this tile's epilogue.
+// Operands use the 128-byte swizzle.  A is K-major (row-major M x K).  B is
+// K-major (stored N x K: symmetric operands and the Gram product) or MN-major
+// (stored K x N: the m x n iterate multiplied from the left).
+//
+// Every mbarrier wait is bounded (about 2 s of %globaltimer); on expiry the
+// waiting thread records DEV_TIMEOUT in the status word and leaves its loop,
+// so a broken pipeline ends the kernel instead of hanging the GPU.
+#include <cuda_bf16.h>
+
+#include "epilogue.cuh"
+
+namespace dmuon {
+namespace {
+
+constexpr int BM = kTcBM;
+constexpr int BN = kTcBN;
+constexpr int STAGES = kTcStages;
+constexpr int SLAB_K = kTcSlabBytes / 2;        // 64 bf16 per 128-byte row
+constexpr int UMMA_K = 16;                      // bf16 K per tcgen05.mma
+constexpr int A_BYTES = BM * kTcSlabBytes;      // 16 KB
+constexpr int B_BYTES = BN * kTcSlabBytes;      // 32 KB
+constexpr int MN_BOX_BYTES = SLAB_K * 128;      // one MN-major box: 64 K-rows x 128 B
+constexpr uint32_t STAGE_TX = A_BYTES + B_BYTES;
+constexpr uint32_t TMEM_COLS = 512;             // two 256-column accumulators
+constexpr uint64_t kWaitNs = 2000000000ull;
+
+struct __align__(1024) Smem {
+    uint8_t a[STAGES][A_BYTES];
+    uint8_t b[STAGES][B_BYTES];
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t acc_full[2];
+    uint64_t acc_empty[2];
+    uint32_t tmem_base;
+    float stage[4][32 * 33];  // per epilogue warp: 32 x 32 chunk, padded rows
+};
+
+__device__ __forceinline__ uint32_t saddr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(saddr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(saddr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Slow path of the bounded wait: polls for about 2 s of %globaltimer.
+__device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, int32_t* status) {
+    const uint64_t t0 = globaltimer();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 256; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer() - t0 > kWaitNs) {
+            atomicExch(status, DEV_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// Bounded wait for the phase of the given parity.  false = timed out.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity, status);
+}
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1,
+                                            int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(saddr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(saddr(bar))
+        : "memory");
+}
+
+// A tensor map written by a host copy must be acquired by the tensormap proxy
+// before TMA reads it.
+__device__ __forceinline__ void tensormap_acquire(const CUtensorMap* map) {
+    asm volatile("fence.proxy.tensormap::generic.acquire.sys [%0], 128;" ::"l"(reinterpret_cast<uint64_t>(map))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor, 128-byte swizzle (sm_100 family format).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((addr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1) << 46;  // descriptor version
+    d |= static_cast<uint64_t>(2) << 61;  // SWIZZLE_128B
+    return d;
+}
+
+// Instruction descriptor: kind::f16, bf16 A/B, fp32 D, M = 128, N = 256.
+__host__ __device__ constexpr uint32_t make_idesc(bool b_mn_major) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+           (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(BM >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(saddr(bar))
+                 : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+          "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+          "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+          "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+struct TileCoord {
+    int gi, mat, tm, tn;
+};
+
+// Static schedule: tile index -> (group, matrix, row tile, column tile).
+// Symmetric groups enumerate row tile i with column tiles 0 .. i/2 (a 256-wide
+// column tile covers two 128-high row tiles), i.e. the lower triangle.
+__device__ __forceinline__ TileCoord decode_tile(const LaunchList& L, int t) {
+    TileCoord c;
+    int gi = 0;
+    while (gi + 1 < L.n && L.begin[gi + 1] <= t) ++gi;
+    const GemmGroup& g = L.groups[L.idx[gi]];
+    const int local = t - L.begin[gi];
+    c.gi = gi;
+    c.mat = local / g.tiles_per_mat;
+    int idx = local % g.tiles_per_mat;
+    if (g.sym) {
+        int i = 0;
+        while (idx >= i / 2 + 1) {
+            idx -= i / 2 + 1;
+            ++i;
+        }
+        c.tm = i;
+        c.tn = idx;
+    } else {
+        c.tm = idx / g.tiles_n;
+        c.tn = idx % g.tiles_n;
+    }
+    return c;
+}
+
+// Epilogue parameters of one tile, held in registers (the group table lives in
+// global memory, and stores through generic pointers would otherwise force
+// the compiler to reload every field after each store).
+struct EpiRegs {
+    const char* aux;
+    char* out[3];
+    char* w;
+    float alpha, c_acc, c_diag, c_aux, lrs, decay;
+    int32_t M, N, mode, sym, aux_type, aux_ld, w_type, w_cols, transposed;
+    int32_t out_ld[3], out_type[3];
+};
+
+__device__ __forceinline__ EpiRegs load_epi(const GemmGroup& g, const LaunchList& L, int mat) {
+    const EpiCtx c = make_epi_ctx(g, L, mat);
+    EpiRegs e;
+    e.aux = static_cast<const char*>(c.aux);
+#pragma unroll
+    for (int o = 0; o < 3; ++o) {
+        e.out[o] = static_cast<char*>(c.out[o]);
+        e.out_ld[o] = g.out_ld[o];
+        e.out_type[o] = g.out_type[o];
+    }
+    e.w = static_cast<char*>(c.w);
+    e.alpha = c.alpha;
+    e.c_acc = g.c_acc;
+    e.c_diag = g.c_diag;
+    e.c_aux = g.c_aux;
+    e.lrs = c.lrs;
+    e.decay = L.decay;
+    e.M = g.M;
+    e.N = g.N;
+    e.mode = g.mode;
+    e.sym = g.sym;
+    e.aux_type = g.aux_type;
+    e.aux_ld = g.aux_ld;
+    e.w_type = c.w_type;
+    e.w_cols = c.w_cols;
+    e.transposed = c.transposed;
+    return e;
+}
+
+// Same formula, same operation order as epi_value (epilogue.cuh).
+__device__ __forceinline__ float epi_v(const EpiRegs& e, int r, int c, float acc, float aux) {
+    float t = e.c_acc * acc;
+    if (r == c) t += e.c_diag;
+    if (e.aux) t = fmaf(e.c_aux, aux, t);
+    return e.alpha * t;
+}
+
+__device__ __forceinline__ void epi_out(const EpiRegs& e, int i, int j, float v) {
+#pragma unroll
+    for (int o = 0; o < 3; ++o)
+        if (e.out[o]) store_elem(e.out[o], static_cast<int64_t>(i) * e.out_ld[o] + j, e.out_type[o], v);
+}
+
+__device__ __forceinline__ void epi_w(const EpiRegs& e, int64_t wi, float v) {
+    const float w = load_elem(e.w, wi, e.w_type);
+    store_elem(e.w, wi, e.w_type, fmaf(-e.lrs, v, e.decay * w));
+}
+
+// One 32 x 32 chunk: rows r0 .. r0+31 (this warp's TMEM lanes), columns
+// c0 .. c0+31.  tcgen05.ld leaves row r0+lane in this thread; the chunk is
+// staged through shared memory so that direct stores, aux reads and W
+// accesses run with lane = column (coalesced rows), while mirrored stores and
+// the transposed W update run with lane = row (coalesced columns).
+__device__ __forceinline__ void epi_chunk(const EpiRegs& e, float* st, int r0, int c0, int lane,
+                                          const float (&acc)[32]) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) st[lane * 33 + j] = acc[j];
+    __syncwarp();
+    const int c = c0 + lane;
+    const bool col_ok = c < e.N;
+    const bool row_pass = (e.mode == EPI_STORE && e.sym) || (e.mode == EPI_UPDATE && e.transposed);
+    const int rows = min(32, e.M - r0);
+    for (int i = 0; i < rows; ++i) {
+        const int r = r0 + i;
+        if (col_ok) {
+            const float aux = e.aux ? load_elem(e.aux, static_cast<int64_t>(r) * e.aux_ld + c, e.aux_type) : 0.0f;
+            const float v = epi_v(e, r, c, st[i * 33 + lane], aux);
+            if (e.mode == EPI_STORE) {
+                if (!e.sym || r >= c) epi_out(e, r, c, v);
+            } else if (!e.transposed) {
+                epi_w(e, static_cast<int64_t>(r) * e.w_cols + c, v);
+            }
+            if (row_pass) st[i * 33 + lane] = v;
+        }
+    }
+    if (row_pass) {
+        __syncwarp();
+        const int r = r0 + lane;
+        if (r < e.M) {
+            const int ncol = min(32, e.N - c0);
+            for (int j = 0; j < ncol; ++j) {
+                const int cc = c0 + j;
+                const float v = st[lane * 33 + j];
+                if (e.mode == EPI_STORE) {
+                    if (r > cc) epi_out(e, cc, r, v);
+                } else {
+                    epi_w(e, static_cast<int64_t>(cc) * e.w_cols + r, v);
+                }
+            }
+        }
+    }
+    __syncwarp();
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_constant__ LaunchList L) {
+    extern __shared__ uint8_t smem_raw[];
+    Smem& S = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&S.full[s], 1);
+            mbar_init(&S.empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&S.acc_full[b], 1);
+            mbar_init(&S.acc_empty[b], 4 * 32);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(&S.tmem_base)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = S.tmem_base;
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------ TMA producer
+        uint32_t stage = 0, phase = 0;
+        uint32_t issued = 0, issued_parity = 0;  // per-stage bit masks
+        bool ok = true;
+        for (int j = 0; j < L.n; ++j) {
+            tensormap_acquire(&L.groups[L.idx[j]].tma_a);
+            tensormap_acquire(&L.groups[L.idx[j]].tma_b);
+        }
+        for (int t = blockIdx.x; t < L.total_tiles && ok; t += gridDim.x) {
+            const TileCoord tc = decode_tile(L, t);
+            const GemmGroup* g = L.groups + L.idx[tc.gi];
+            const int nkb = (g->K + SLAB_K - 1) / SLAB_K;
+            for (int kb = 0; kb < nkb; ++kb) {
+                if (!mbar_wait(&S.empty[stage], phase ^ 1, L.status)) {
+                    ok = false;
+                    break;
+                }
+                mbar_expect_tx(&S.full[stage], STAGE_TX);
+                issued |= 1u << stage;
+                issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                tma_load_3d(S.a[stage], &g->tma_a, &S.full[stage], kb * SLAB_K, tc.tm * BM, tc.mat);
+                if (!g->b_mn_major) {
+                    tma_load_3d(S.b[stage], &g->tma_b, &S.full[stage], kb * SLAB_K, tc.tn * BN, tc.mat);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < BN / 64; ++i)
+                        tma_load_3d(S.b[stage] + i * MN_BOX_BYTES, &g->tma_b, &S.full[stage], tc.tn * BN + 64 * i,
+                                    kb * SLAB_K, tc.mat);
+                }
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+        }
+        if (!ok) {
+            // let copies already issued land before the CTA can exit
+            for (int s = 0; s < STAGES; ++s)
+                if (issued & (1u << s)) mbar_wait(&S.full[s], (issued_parity >> s) & 1u, L.status);
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ------------------------------------------------ MMA issuer
+        uint32_t stage = 0, phase = 0;
+        bool ok = true;
+        int it = 0;
+        for (int t = blockIdx.x; t < L.total_tiles && ok; t += gridDim.x, ++it) {
+            const TileCoord tc = decode_tile(L, t);
+            const GemmGroup* g = L.groups + L.idx[tc.gi];
+            const int nkb = (g->K + SLAB_K - 1) / SLAB_K;
+            const int buf = it & 1;
+            const uint32_t use = static_cast<uint32_t>(it >> 1);
+            if (!mbar_wait(&S.acc_empty[buf], (use & 1) ^ 1, L.status)) break;
+            tc_fence_after();
+            const uint32_t d = tmem + static_cast<uint32_t>(buf * BN);
+            const bool bmn = g->b_mn_major != 0;
+            const uint32_t idesc = make_idesc(bmn);
+            for (int kb = 0; kb < nkb; ++kb) {
+                if (!mbar_wait(&S.full[stage], phase, L.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a0 = saddr(S.a[stage]);
+                const uint32_t b0 = saddr(S.b[stage]);
+#pragma unroll
+                for (int kk = 0; kk < SLAB_K / UMMA_K; ++kk) {
+                    const uint64_t ad = smem_desc(a0 + kk * (UMMA_K * 2), 0, 1024);
+                    const uint64_t bd = bmn ? smem_desc(b0 + kk * (UMMA_K * 128), MN_BOX_BYTES, 1024)
+                                            : smem_desc(b0 + kk * (UMMA_K * 2), 0, 1024);
+                    umma_bf16(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+                }
+                umma_commit(&S.empty[stage]);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+            // also on failure: the commit tracks every MMA issued so far, so the
+            // epilogue's wait on it covers them before TMEM is released
+            umma_commit(&S.acc_full[buf]);
+        }
+    } else if (warp >= 2) {
+        // ------------------------------------------------ epilogue
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        int it = 0;
+        for (int t = blockIdx.x; t < L.total_tiles; t += gridDim.x, ++it) {
+            const TileCoord tc = decode_tile(L, t);
+            const GemmGroup& g = L.groups[L.idx[tc.gi]];
+            const int buf = it & 1;
+            const uint32_t use = static_cast<uint32_t>(it >> 1);
+            if (!mbar_wait(&S.acc_full[buf], use & 1, L.status)) break;
+            tc_fence_after();
+            const EpiRegs e = load_epi(g, L, tc.mat);
+            const int r0 = tc.tm * BM + q * 32;
+            const int row_last = tc.tm * BM + BM - 1;
+            float* st = S.stage[warp - 2];
+            for (int ch = 0; ch < BN / 32; ++ch) {
+                const int c0 = tc.tn * BN + ch * 32;
+                if (c0 >= e.N) break;
+                if (e.sym && e.mode == EPI_STORE && c0 > row_last) break;
+                float v[32];
+                __syncwarp();
+                tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN + ch * 32), v);
+                if (r0 < e.M) epi_chunk(e, st, r0, c0, lane, v);
+            }
+            __syncwarp();
+            tc_fence_before();
+            mbar_arrive(&S.acc_empty[buf]);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+    }
+}
+
+}  // namespace
+
+size_t gemm_tc_smem_bytes() { return sizeof(Smem) + 1024; }
+
+cudaError_t launch_gemm_tc(const LaunchList& l, int num_sms, cudaStream_t s) {
+    if (l.total_tiles <= 0) return cudaSuccess;
+    static bool attr_set = false;
+    const size_t smem = gemm_tc_smem_bytes();
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    const int grid = l.total_tiles < num_sms ? l.total_tiles : num_sms;
+    gemm_tc_kernel<<<grid, kTcThreads, smem, s>>>(l);
+    return cudaGetLastError();
+}
+
+}  // namespace dmuon

@@ -1,0 +1,128 @@
+// Internal structures shared by the planner, the runtime and the kernels of
+// the batched Gram-space Newton-Schulz Muon step.  Not part of the C ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace dmuon {
+
+// ---------------------------------------------------------------- constants
+
+// tcgen05 GEMM tile: 128 rows (TMEM lanes) x 256 columns, 128-byte K slabs.
+constexpr int kTcBM = 128;
+constexpr int kTcBN = 256;
+constexpr int kTcSlabBytes = 128;  // one K slab row = one 128-byte swizzle row
+constexpr int kTcStages = 4;
+constexpr int kTcThreads = 192;    // warp 0 TMA, warp 1 MMA + TMEM, warps 2-5 epilogue
+
+// fp32 FFMA GEMM tile
+constexpr int kSimtBM = 64;
+constexpr int kSimtBN = 64;
+constexpr int kSimtThreads = 256;
+
+// momentum / pack tile over the original (rows x cols) matrix
+constexpr int kMomTile = 64;
+constexpr int kMomThreads = 256;
+
+constexpr int kMaxGroupsPerLaunch = 96;
+
+enum ElemType : int32_t { ELEM_BF16 = 0, ELEM_F32 = 1 };
+enum EpiMode : int32_t { EPI_STORE = 0, EPI_UPDATE = 1 };
+enum AlphaSel : int32_t { ALPHA_ONE = 0, ALPHA_INV = 1, ALPHA_INV2 = 2 };
+
+// Device status word values (first int32 of the workspace).
+enum DevStatus : int32_t { DEV_OK = 0, DEV_TIMEOUT = 1 };
+
+// ---------------------------------------------------------------- tables
+
+// Per matrix of the plan, in bucket order ("slot").
+struct MatInfo {
+    void* x;            // packed u: m x ldx, row-major, transposed for tall matrices
+    float* partials;    // sum-of-squares partials, one per momentum tile
+    int64_t ldx;        // elements
+    int64_t tile_begin; // first momentum tile of this slot inside its wave
+    int64_t gidx;       // index of the matrix in the caller's arrays
+    int32_t rows, cols; // original shape
+    int32_t tiles_c;    // momentum tiles along cols
+    int32_t ntiles;     // momentum tiles of this matrix
+    int32_t transposed; // rows > cols
+    int32_t dtype;      // storage dtype of W, grad, momentum (ElemType)
+    int32_t x_type;     // ElemType of the packed u
+    float scale;        // update shape scale s
+};
+
+struct SlotScalars {
+    float inv;   // 1 / (||u||_F + eps)
+    float inv2;  // inv^2
+};
+
+// One batched product D[mat] = A[mat] (M x K) * B[mat] (K x N) with a fused
+// epilogue.  A is K-major (row-major M x K).  The B operand is K-major (stored
+// N x K) or MN-major (stored K x N).  Built on the host, read by the kernels.
+struct GemmGroup {
+    CUtensorMap tma_a;      // tcgen05 path: A as {K, M, batch}
+    CUtensorMap tma_b;      // K-major {K, N, batch} or MN-major {N, K, batch}
+    // raw views (fp32 FFMA path)
+    const void* a;
+    const void* b;
+    int64_t a_bs, b_bs;     // batch strides, elements
+    int32_t lda, ldb;
+    int32_t a_type, b_type; // ElemType
+    int32_t M, N, K, batch;
+    int32_t b_mn_major;
+    int32_t sym;            // symmetric D: lower-triangle tiles, mirrored stores
+    int32_t tiles_m, tiles_n, tiles_per_mat;
+    int32_t slot_base;      // slot of batch entry 0
+    // epilogue: v = alpha * (c_acc*acc + c_diag*[r==c] + c_aux*aux[r][c])
+    int32_t mode;           // EpiMode
+    int32_t alpha_sel;      // AlphaSel
+    float c_acc, c_diag, c_aux;
+    int32_t aux_type;       // ElemType
+    int32_t aux_sym;        // aux is bitwise symmetric: read aux[c][r] (coalesced)
+    int32_t aux_ld;
+    const void* aux;
+    int64_t aux_bs;
+    // up to three stored copies of v (EPI_STORE), each with its own dtype
+    void* out[3];
+    int64_t out_bs[3];
+    int32_t out_ld[3];
+    int32_t out_type[3];
+};
+
+// Passed by value to every GEMM launch.
+struct LaunchList {
+    const GemmGroup* groups;                 // device table base
+    const MatInfo* infos;                    // device, indexed by slot
+    const SlotScalars* scalars;              // device, indexed by slot
+    void* const* params;                     // device, indexed by gidx
+    int32_t* status;                         // device status word
+    float lr, decay;                         // update: W = decay*W - lr*s*v
+    int32_t n;                               // groups in this launch
+    int32_t total_tiles;
+    int32_t idx[kMaxGroupsPerLaunch];        // indices into `groups`
+    int32_t begin[kMaxGroupsPerLaunch + 1];  // tile prefix
+};
+
+struct MomentumArgs {
+    const MatInfo* infos;    // slots of the wave, first one at infos[0]
+    SlotScalars* scalars;    // same slots
+    const void* const* grads;
+    void* const* moms;
+    int32_t nslots;
+    int64_t total_tiles;
+    float beta;
+    int32_t nesterov;
+    float eps;
+};
+
+// ---------------------------------------------------------------- launchers
+
+cudaError_t launch_momentum_pack(const MomentumArgs& a, cudaStream_t s);
+cudaError_t launch_norm_finalize(const MomentumArgs& a, cudaStream_t s);
+cudaError_t launch_gemm_tc(const LaunchList& l, int num_sms, cudaStream_t s);
+cudaError_t launch_gemm_simt(const LaunchList& l, cudaStream_t s);
+size_t gemm_tc_smem_bytes();
+
+}  // namespace dmuon

@@ -11,7 +11,7 @@ C ABI header ``include/dmuon.h`` states for ``dmuon_plan``:
   (rows > cols) are packed transposed;
 * buckets keyed (dtype, m, n), ascending; input order inside a bucket;
 * route per bucket: FP32 precision -> Gram unless forced; AUTO -> Gram when
-  n >= 2m or m <= small_m, else direct;
+  n >= 3m or m <= small_m, else direct;
 * m x m engine: FP32 precision -> fp32 FFMA; BF16 precision -> fp32 FFMA for
   Gram buckets with m <= small_m, tensor cores otherwise;
 * per-matrix workspace bytes: the sum of the per-matrix buffers below, each
@@ -78,7 +78,7 @@ def plan_buckets(shapes, precision: int = PREC_BF16, route: int = ROUTE_AUTO,
         elif route == ROUTE_DIRECT:
             r = BUCKET_DIRECT
         else:
-            r = BUCKET_GRAM if (n >= 2 * m or (small_m > 0 and m <= small_m)) else BUCKET_DIRECT
+            r = BUCKET_GRAM if (n >= 3 * m or (small_m > 0 and m <= small_m)) else BUCKET_DIRECT
         if precision == PREC_FP32:
             eng = ENGINE_SIMT_FP32
         elif r == BUCKET_GRAM and small_m > 0 and m <= small_m:

@@ -1,0 +1,236 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Tolerances (relative Frobenius error of the orthogonalised update O): 3e-2 in
+bf16 mode (tensor cores, bf16 operands, fp32 accumulation), 1e-4 in the fp32
+validation mode.  Momentum: every element within 1 ulp of the oracle's single
+rounding (the kernel rounds fl32(beta*M + grad) once more).  Parameters: every
+element within one ulp plus the recovery rounding of O_gpu of
+RN((1 - lr*wd) W - lr*s*O_gpu), O_gpu recovered through the ABI from the same
+inputs, and 99 % within one ulp.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from tests.helpers import TOL, f32, gpu_O, oracle_O, rel_fro, run_step, storage, ulp_diff, ulp_of
+
+pytestmark = pytest.mark.gpu
+
+BETA, LR, WD = f32(0.95), f32(0.02), f32(0.01)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+
+
+def make_inputs(shapes, dtype, seed, grad_scale=1e-3, mom_std=1e-3):
+    cfg = workloads.Config("t", "test", dtype, seed, tuple(shapes), "normal", grad_scale=grad_scale,
+                           mom_std=mom_std)
+    return [workloads.make_matrix(cfg, i, "cpu") for i in range(len(shapes))]
+
+
+def check_O(shapes, inputs, dtype, tol=None, ns_steps=5, **kw):
+    got, muon = gpu_O(shapes, inputs, dtype, beta=BETA, ns_steps=ns_steps, **kw)
+    want = oracle_O(inputs, beta=BETA, ns_steps=ns_steps)
+    errs = [rel_fro(g, w) for g, w in zip(got, want)]
+    if tol is None:
+        tol = TOL["fp32"] if kw.get("precision", "bf16") == "fp32" else TOL["bf16"]
+    worst = int(np.argmax(errs))
+    assert errs[worst] <= tol, f"{shapes[worst]}: rel err {errs[worst]:.3e} > {tol}"
+    return errs, muon
+
+
+# ------------------------------------------------------------------ small and ragged
+
+RAGGED = [(8, 16), (16, 8), (65, 130), (130, 65), (33, 33), (1, 37), (37, 1), (3, 500), (300, 300),
+          (320, 704), (704, 320), (257, 600), (520, 1100), (1100, 520), (400, 520)]
+
+
+def test_ragged_shapes_bf16():
+    inputs = make_inputs(RAGGED, "bf16", 11)
+    check_O(RAGGED, inputs, "bf16")
+
+
+def test_ragged_shapes_fp32_validation():
+    inputs = make_inputs(RAGGED, "fp32", 12)
+    check_O(RAGGED, inputs, "fp32", precision="fp32")
+
+
+def test_bf16_storage_fp32_validation_mode():
+    # O is only visible through bf16 parameters here, so compare the stored
+    # bits: fp32 arithmetic (error ~1e-6) rounds to the same bf16 as the oracle
+    # up to one ulp where the exact value sits near a rounding boundary.
+    shapes = [(96, 200), (200, 96), (150, 150), (320, 330)]
+    inputs = make_inputs(shapes, "bf16", 13)
+    w, _, _ = run_step(shapes, inputs, "bf16", lr=1.0, beta=BETA, wd=0.0, zero_w=True, precision="fp32")
+    want = oracle_O(inputs, beta=BETA)
+    for (r, c), wi, o in zip(shapes, w, want):
+        s = oracle.shape_scale(r, c)
+        ref = oracle.round_to_bf16(-s * o)
+        # one bf16 ulp, plus the fp32 path's own error (1e-4 of the rms of s*O)
+        # for elements near zero, whose ulp is far below that
+        slack = 1e-4 * s * np.sqrt(np.mean(o * o))
+        assert np.all(np.abs(wi.double().numpy() - ref) <= ulp_of(ref, "bf16") + slack), (r, c)
+        d = ulp_diff(wi, torch.from_numpy(ref).to(torch.bfloat16))
+        assert (d == 0).mean() > 0.99, (r, c)
+
+
+@pytest.mark.parametrize("route", ["gram", "direct"])
+def test_forced_routes_rectangular(route):
+    shapes = [(320, 704), (704, 320), (288, 1024), (64, 300)]
+    inputs = make_inputs(shapes, "bf16", 14)
+    check_O(shapes, inputs, "bf16", route=route, small_m=-1)
+
+
+@pytest.mark.parametrize("ns_steps", [1, 2, 3, 4, 6])
+def test_ns_step_counts(ns_steps):
+    shapes = [(320, 704), (300, 320), (48, 200), (200, 48)]
+    inputs = make_inputs(shapes, "bf16", 15)
+    check_O(shapes, inputs, "bf16", ns_steps=ns_steps)
+
+
+def test_momentum_and_update_ulps():
+    shapes = [(320, 704), (704, 320), (300, 300), (48, 200), (65, 130)]
+    for dtype in ("bf16", "fp32"):
+        inputs = make_inputs(shapes, dtype, 16)
+        prec = "bf16" if dtype == "bf16" else "fp32"
+        w_new, m_new, _ = run_step(shapes, inputs, dtype, lr=LR, beta=BETA, wd=WD, precision=prec)
+        o_gpu, _ = gpu_O(shapes, inputs, dtype, beta=BETA, precision=prec)
+        st = storage(dtype)
+        for i, (w, g, m) in enumerate(inputs):
+            r, c = shapes[i]
+            want_m = oracle.round_to_storage(BETA * m.double().numpy() + g.double().numpy(), dtype)
+            assert ulp_diff(m_new[i], torch.from_numpy(want_m).to(st)).max() <= 1
+            s = oracle.shape_scale(r, c)
+            # The update applied to the kernel's own O.  o_gpu went through one
+            # rounding to the storage dtype (relative 2^-9 for bf16, 2^-24 for
+            # fp32), so each element may differ from the kernel's internal fp32
+            # value by that much times lr*s*|O|, plus the final rounding.
+            w64 = w.double().numpy()
+            exact = (1 - LR * WD) * w64 - LR * s * o_gpu[i]
+            want_w = oracle.round_to_storage(exact, dtype)
+            got = w_new[i].double().numpy()
+            # fp32 arithmetic in the kernel (decay*W and lr*s rounded, one fma)
+            # costs up to about one ulp of max(|W|, |W'|); the recovered O adds
+            # its own rounding (2^-9 bf16, 2^-24 fp32) times lr*s*|O|
+            unit = 2.0 ** -8 if dtype == "bf16" else 2.0 ** -23
+            big = np.maximum(np.abs(want_w), np.abs(w64))
+            bound = ulp_of(want_w, dtype) + ulp_of(big, "fp32") * 2 + 2 * unit * LR * s * np.abs(o_gpu[i])
+            assert np.all(np.abs(got - want_w) <= bound), (shapes[i], dtype)
+            d = ulp_diff(w_new[i], torch.from_numpy(want_w).to(st))
+            assert (d <= 1).mean() >= 0.99, (shapes[i], dtype)
+
+
+def test_zero_gradient_gives_pure_decay():
+    shapes = [(320, 704), (48, 200), (300, 300)]
+    inputs = [(w, torch.zeros_like(g), torch.zeros_like(m)) for w, g, m in make_inputs(shapes, "bf16", 17)]
+    w_new, m_new, _ = run_step(shapes, inputs, "bf16", lr=LR, beta=BETA, wd=WD)
+    for i, (w, _, _) in enumerate(inputs):
+        want = oracle.round_to_bf16((1 - LR * WD) * w.double().numpy())
+        assert ulp_diff(w_new[i], torch.from_numpy(want).to(torch.bfloat16)).max() <= 1
+        assert torch.all(m_new[i] == 0)
+
+
+def test_nesterov_off_and_rms_scale():
+    shapes = [(320, 704), (704, 320), (48, 200)]
+    inputs = make_inputs(shapes, "bf16", 18)
+    got, _ = gpu_O(shapes, inputs, "bf16", beta=BETA, nesterov=False, scale_rule="rms")
+    want = oracle_O(inputs, beta=BETA, nesterov=False)
+    for g, w in zip(got, want):
+        assert rel_fro(g, w) <= 3e-2
+
+
+def test_deterministic_and_batching_invariant():
+    shapes = [(320, 704)] * 3 + [(48, 200)] * 3 + [(300, 300)] * 2
+    inputs = make_inputs(shapes, "bf16", 19)
+    a, _, _ = run_step(shapes, inputs, "bf16", lr=LR, beta=BETA, wd=WD)
+    b, _, _ = run_step(shapes, inputs, "bf16", lr=LR, beta=BETA, wd=WD)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+    # each matrix alone gives the same bits as inside its bucket
+    for i in (1, 4, 7):
+        alone, _, _ = run_step([shapes[i]], [inputs[i]], "bf16", lr=LR, beta=BETA, wd=WD)
+        assert torch.equal(alone[0], a[i])
+
+
+def test_gram_buffer_bitwise_symmetric():
+    # the last Gram-route R and the last direct-route A = X X^T are stored as
+    # lower triangle plus mirror, so they are bitwise symmetric
+    shapes = [(320, 704)] * 2 + [(300, 960)] + [(520, 1100)]
+    inputs = make_inputs(shapes, "bf16", 20)
+    _, _, muon = run_step(shapes, inputs, "bf16", lr=LR, beta=BETA, wd=WD)
+    ws = muon.workspace
+    buckets = muon.buckets()
+    assert {b["route"] for b in buckets} == {1, 2}
+    for p, (bi, start, nb) in enumerate(muon.waves()[0]):
+        m = buckets[bi]["m"]
+        off, ld, bs = muon.debug_buffer(0, p, 1)
+        raw = ws[off: off + nb * bs * 4].view(torch.float32).cpu().view(nb, bs)
+        for j in range(nb):
+            r = raw[j, : m * ld].view(m, ld)[:, :m]
+            assert torch.equal(r, r.t())
+            assert torch.isfinite(r).all()
+
+
+def test_workspace_budget_waves():
+    shapes = [(320, 704)] * 5 + [(300, 300)] * 3 + [(48, 200)] * 4
+    inputs = make_inputs(shapes, "bf16", 21)
+    full, _, _ = run_step(shapes, inputs, "bf16", lr=LR, beta=BETA, wd=WD)
+    from matrix_orthogonalising_optimizer_gb300 import Muon
+    probe = Muon([(r, c, 0) for r, c in shapes])
+    big = max(b["per_matrix_bytes"] for b in probe.buckets())
+    waved, _, muon = run_step(shapes, inputs, "bf16", lr=LR, beta=BETA, wd=WD, workspace_budget=2 * big)
+    assert len(muon.waves()) > 2
+    for x, y in zip(full, waved):
+        assert torch.equal(x, y)
+
+
+def test_timing_counts_launches():
+    shapes = [(320, 704), (48, 200), (300, 300)]
+    inputs = make_inputs(shapes, "bf16", 22)
+    from matrix_orthogonalising_optimizer_gb300 import Muon
+    muon = Muon([(r, c, 0) for r, c in shapes]).bind()
+    muon.set_timing(True)
+    run_step(shapes, inputs, "bf16", lr=LR, beta=BETA, wd=WD, muon=muon)
+    t = muon.timing()
+    assert t["momentum"][1] == 1 and t["norm"][1] == 1
+    assert t["tc"][1] > 0 and t["simt"][1] > 0
+    assert all(v[0] >= 0 for v in t.values())
+
+
+# ------------------------------------------------------------------ configurations
+
+
+def test_c1_single_fp32():
+    cfg = workloads.get("c1")
+    inputs = [workloads.make_matrix(cfg, 0, "cpu")]
+    errs, _ = check_O(list(cfg.shapes), inputs, "fp32", precision="fp32")
+    assert errs[0] <= 1e-4
+
+
+def test_c2_small_transformer():
+    cfg = workloads.get("c2")
+    inputs = [workloads.make_matrix(cfg, i, "cpu") for i in range(len(cfg.shapes))]
+    errs, muon = check_O(list(cfg.shapes), inputs, "bf16")
+    assert len(muon.buckets()) == 3
+
+
+def test_c4_heterogeneous_sampled():
+    cfg = workloads.get("c4")
+    shapes = list(cfg.shapes)
+    inputs = [workloads.make_matrix(cfg, i, "cpu") for i in range(len(shapes))]
+    got, muon = gpu_O(shapes, inputs, "bf16", beta=BETA)
+    # every bucket's first member, plus a seeded sample
+    picks = {b["members"][0] for b in muon.buckets()}
+    rng = np.random.default_rng(3)
+    picks |= set(int(i) for i in rng.choice(len(shapes), 60, replace=False))
+    picks = sorted(picks)
+    want = oracle_O([inputs[i] for i in picks], beta=BETA)
+    errs = [rel_fro(got[i], w) for i, w in zip(picks, want)]
+    assert max(errs) <= 3e-2, max(errs)

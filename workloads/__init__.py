@@ -66,6 +66,11 @@ CONFIGS = {
                  _layers(32, ((4096, 4096), (1024, 4096), (1024, 4096), (4096, 4096),
                               (14336, 4096), (14336, 4096), (4096, 14336))),
                  "heavy", grad_scale=1e-3),
+    # two layers of the c3 shapes: the same kernels on a few GB, for profiler captures
+    "c3x2": Config("c3x2", "Llama-3-8B-shaped set, 2 x {q, k, v, o, gate, up, down}", "bf16", 2,
+                   _layers(2, ((4096, 4096), (1024, 4096), (1024, 4096), (4096, 4096),
+                               (14336, 4096), (14336, 4096), (4096, 14336))),
+                   "heavy", grad_scale=1e-3),
     "c4": Config("c4", "embodied/VLA-like heterogeneous set, 2000 matrices", "bf16", 3,
                  _vla_shapes(3), "logscale", logscale=(-5.0, -1.0)),
     "c5": Config("c5", "large-layer stress, 80 x {8192x8192, 28672x8192, 8192x28672}", "bf16", 4,
