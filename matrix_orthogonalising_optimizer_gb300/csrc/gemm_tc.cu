@@ -15,7 +15,8 @@
 //   warp 1      allocates 512 TMEM columns; one thread issues tcgen05.mma
 //               (kind::f16, bf16 operands, fp32 accumulation) into one of two
 //               128 x 256 fp32 accumulators
-//   warps 2..5  epilogue: tcgen05.ld the accumulator (row per thread), apply
+//   warps 2..9  epilogue, two per TMEM lane quarter (128 columns each):
+//               tcgen05.ld the accumulator (row per thread), apply
 //               the fused epilogue, store; releases the accumulator so the
 //               next tile's MMAs overlap this tile's epilogue.
 // Operands use the 128-byte swizzle.  A is K-major (row-major M x K).  B is
@@ -43,6 +44,7 @@ constexpr int MN_BOX_BYTES = SLAB_K * 128;      // one MN-major box: 64 K-rows x
 constexpr uint32_t STAGE_TX = A_BYTES + B_BYTES;
 constexpr uint32_t TMEM_COLS = 512;             // two 256-column accumulators
 constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr int CH = 16;                          // epilogue chunk: columns per tcgen05.ld
 
 struct __align__(1024) Smem {
     uint8_t a[STAGES][A_BYTES];
@@ -52,7 +54,6 @@ struct __align__(1024) Smem {
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
     uint32_t tmem_base;
-    float stage[4][32 * 33];  // per epilogue warp: 32 x 32 chunk, padded rows
 };
 
 __device__ __forceinline__ uint32_t saddr(const void* p) {
@@ -91,7 +92,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Slow path of the bounded wait: polls for about 2 s of %globaltimer.
-__device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, int32_t* status) {
+__device__ __forceinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, int32_t* status) {
     const uint64_t t0 = globaltimer();
     while (true) {
 #pragma unroll 1
@@ -161,22 +162,18 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
                  : "memory");
 }
 
-// 32 consecutive fp32 columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-    uint32_t r[32];
+// CH = 16 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[CH]) {
+    uint32_t r[16];
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
-          "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
-          "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
-          "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 struct TileCoord {
@@ -204,8 +201,16 @@ __device__ __forceinline__ TileCoord decode_tile(const LaunchList& L, int t) {
         c.tm = i;
         c.tn = idx;
     } else {
-        c.tm = idx / g.tiles_n;
-        c.tn = idx % g.tiles_n;
+        // Panels of kPanel column tiles, row tiles inside a panel: a wave of
+        // 152 CTAs then covers about 19 x 8 tiles, whose A rows and B columns
+        // stay in L2, instead of re-streaming all of B once per row of tiles.
+        constexpr int kPanel = 8;
+        const int panel_tiles = g.tiles_m * kPanel;
+        const int panel = idx / panel_tiles;
+        const int within = idx - panel * panel_tiles;
+        const int width = min(kPanel, g.tiles_n - panel * kPanel);
+        c.tm = within / width;
+        c.tn = panel * kPanel + within % width;
     }
     return c;
 }
@@ -218,7 +223,7 @@ struct EpiRegs {
     char* out[3];
     char* w;
     float alpha, c_acc, c_diag, c_aux, lrs, decay;
-    int32_t M, N, mode, sym, aux_type, aux_ld, w_type, w_cols, transposed;
+    int32_t M, N, mode, sym, aux_type, aux_sym, aux_ld, w_type, w_cols, transposed, w_vec;
     int32_t out_ld[3], out_type[3];
 };
 
@@ -244,10 +249,13 @@ __device__ __forceinline__ EpiRegs load_epi(const GemmGroup& g, const LaunchList
     e.mode = g.mode;
     e.sym = g.sym;
     e.aux_type = g.aux_type;
+    e.aux_sym = g.aux_sym;
     e.aux_ld = g.aux_ld;
     e.w_type = c.w_type;
     e.w_cols = c.w_cols;
     e.transposed = c.transposed;
+    // 16-byte row access to W needs every row start on 16 bytes
+    e.w_vec = c.w && ((static_cast<int64_t>(c.w_cols) * (c.w_type == ELEM_BF16 ? 2 : 4)) % 16 == 0);
     return e;
 }
 
@@ -259,61 +267,155 @@ __device__ __forceinline__ float epi_v(const EpiRegs& e, int r, int c, float acc
     return e.alpha * t;
 }
 
-__device__ __forceinline__ void epi_out(const EpiRegs& e, int i, int j, float v) {
+// 8 consecutive elements at p[i .. i+7] (16- or 32-byte aligned).
+__device__ __forceinline__ void ld8(const char* p, int64_t i, int32_t t, float* v) {
+    if (t == ELEM_BF16) {
+        const uint4 q = *reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p) + i);
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&q);
 #pragma unroll
-    for (int o = 0; o < 3; ++o)
-        if (e.out[o]) store_elem(e.out[o], static_cast<int64_t>(i) * e.out_ld[o] + j, e.out_type[o], v);
+        for (int k = 0; k < 4; ++k) {
+            const float2 f = __bfloat1622float2(h[k]);
+            v[2 * k] = f.x;
+            v[2 * k + 1] = f.y;
+        }
+    } else {
+        const float4* q = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(p) + i);
+        const float4 a = q[0], b = q[1];
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    }
 }
 
-__device__ __forceinline__ void epi_w(const EpiRegs& e, int64_t wi, float v) {
-    const float w = load_elem(e.w, wi, e.w_type);
-    store_elem(e.w, wi, e.w_type, fmaf(-e.lrs, v, e.decay * w));
+__device__ __forceinline__ void st8(char* p, int64_t i, int32_t t, const float* v) {
+    if (t == ELEM_BF16) {
+        uint4 q;
+        __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&q);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) h[k] = __floats2bfloat162_rn(v[2 * k], v[2 * k + 1]);
+        *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p) + i) = q;
+    } else {
+        float4* q = reinterpret_cast<float4*>(reinterpret_cast<float*>(p) + i);
+        q[0] = make_float4(v[0], v[1], v[2], v[3]);
+        q[1] = make_float4(v[4], v[5], v[6], v[7]);
+    }
 }
 
-// One 32 x 32 chunk: rows r0 .. r0+31 (this warp's TMEM lanes), columns
-// c0 .. c0+31.  tcgen05.ld leaves row r0+lane in this thread; the chunk is
-// staged through shared memory so that direct stores, aux reads and W
-// accesses run with lane = column (coalesced rows), while mirrored stores and
-// the transposed W update run with lane = row (coalesced columns).
-__device__ __forceinline__ void epi_chunk(const EpiRegs& e, float* st, int r0, int c0, int lane,
-                                          const float (&acc)[32]) {
+// The epilogue works on this thread's row r, columns c0 .. c0+CH-1
+// (tcgen05.ld leaves one row per thread).  Row segments move as 16-byte
+// vectors; the mirrored stores of symmetric results, the symmetric aux reads
+// and the transposed W update use the other orientation, where the warp's 32
+// lanes cover 32 consecutive rows and each access is coalesced.
+//
+// Inputs of a chunk (aux or W) do not depend on the accumulator, so they are
+// loaded one chunk ahead: the first chunk's before the wait for the MMAs, the
+// next chunk's before the current chunk's stores.
+
+// CH elements of row r from columns c0.. of a row-major matrix (or of its
+// transpose when by_col: element (r, c) read at [c][r]).
+__device__ __forceinline__ void load_row(const char* base, int32_t type, int32_t ld, bool by_col, bool vec,
+                                         int r, int c0, int ncol, float (&x)[CH]) {
+    if (by_col) {
 #pragma unroll
-    for (int j = 0; j < 32; ++j) st[lane * 33 + j] = acc[j];
-    __syncwarp();
-    const int c = c0 + lane;
-    const bool col_ok = c < e.N;
-    const bool row_pass = (e.mode == EPI_STORE && e.sym) || (e.mode == EPI_UPDATE && e.transposed);
-    const int rows = min(32, e.M - r0);
-    for (int i = 0; i < rows; ++i) {
-        const int r = r0 + i;
-        if (col_ok) {
-            const float aux = e.aux ? load_elem(e.aux, static_cast<int64_t>(r) * e.aux_ld + c, e.aux_type) : 0.0f;
-            const float v = epi_v(e, r, c, st[i * 33 + lane], aux);
-            if (e.mode == EPI_STORE) {
-                if (!e.sym || r >= c) epi_out(e, r, c, v);
-            } else if (!e.transposed) {
-                epi_w(e, static_cast<int64_t>(r) * e.w_cols + c, v);
-            }
-            if (row_pass) st[i * 33 + lane] = v;
-        }
+        for (int j = 0; j < CH; ++j)
+            x[j] = j < ncol ? load_elem(base, static_cast<int64_t>(c0 + j) * ld + r, type) : 0.0f;
+    } else if (vec) {
+#pragma unroll
+        for (int j = 0; j < CH; j += 8) ld8(base, static_cast<int64_t>(r) * ld + c0 + j, type, x + j);
+    } else {
+#pragma unroll
+        for (int j = 0; j < CH; ++j)
+            x[j] = j < ncol ? load_elem(base, static_cast<int64_t>(r) * ld + c0 + j, type) : 0.0f;
     }
-    if (row_pass) {
-        __syncwarp();
-        const int r = r0 + lane;
-        if (r < e.M) {
-            const int ncol = min(32, e.N - c0);
-            for (int j = 0; j < ncol; ++j) {
-                const int cc = c0 + j;
-                const float v = st[lane * 33 + j];
-                if (e.mode == EPI_STORE) {
-                    if (r > cc) epi_out(e, cc, r, v);
-                } else {
-                    epi_w(e, static_cast<int64_t>(cc) * e.w_cols + r, v);
-                }
+}
+
+// Prefetched input of a chunk: W for the update, else the aux operand.
+__device__ __forceinline__ void epi_load(const EpiRegs& e, int r, int c0, float (&x)[CH]) {
+    if (r >= e.M || c0 >= e.N) return;
+    const int ncol = min(CH, e.N - c0);
+    const bool full = ncol == CH;
+    const char* base;
+    int32_t type, ld;
+    bool by_col;
+    bool vec;
+    if (e.mode == EPI_UPDATE) {
+        base = e.w;
+        type = e.w_type;
+        ld = e.w_cols;
+        by_col = e.transposed;
+        vec = full && e.w_vec;
+    } else if (e.aux) {
+        base = e.aux;
+        type = e.aux_type;
+        ld = e.aux_ld;
+        by_col = e.aux_sym;
+        vec = full;
+    } else {
+        return;
+    }
+    load_row(base, type, ld, by_col, vec, r, c0, ncol, x);
+}
+
+// v (computed in place of the accumulator values) and, for the update, the new
+// W (in place of the loaded W values), to keep the register footprint low.
+__device__ __forceinline__ void epi_finish(const EpiRegs& e, int r, int c0, float (&v)[CH], float (&x)[CH]) {
+    if (r >= e.M) return;
+    const int ncol = min(CH, e.N - c0);
+    const bool full = ncol == CH;
+    const bool upd = e.mode == EPI_UPDATE;
+    if (upd && e.aux) {
+        // the update that also has an aux term (direct route: a X + B X) reads
+        // the aux chunk here; x already holds W
+        float a[CH];
+        load_row(e.aux, e.aux_type, e.aux_ld, e.aux_sym, full, r, c0, ncol, a);
+#pragma unroll
+        for (int j = 0; j < CH; ++j) v[j] = epi_v(e, r, c0 + j, v[j], a[j]);
+    } else {
+#pragma unroll
+        for (int j = 0; j < CH; ++j) v[j] = epi_v(e, r, c0 + j, v[j], upd ? 0.0f : x[j]);
+    }
+
+    if (!upd) {
+        const bool below = !e.sym || c0 + CH - 1 < r;  // every column of the chunk is stored directly
+#pragma unroll
+        for (int o = 0; o < 3; ++o) {
+            if (!e.out[o]) continue;
+            const int64_t rb = static_cast<int64_t>(r) * e.out_ld[o];
+            if (full && below) {
+#pragma unroll
+                for (int j = 0; j < CH; j += 8) st8(e.out[o], rb + c0 + j, e.out_type[o], v + j);
+            } else {
+#pragma unroll
+                for (int j = 0; j < CH; ++j)
+                    if (j < ncol && (!e.sym || r >= c0 + j)) store_elem(e.out[o], rb + c0 + j, e.out_type[o], v[j]);
+            }
+            if (e.sym) {
+#pragma unroll
+                for (int j = 0; j < CH; ++j)
+                    if (j < ncol && r > c0 + j)
+                        store_elem(e.out[o], static_cast<int64_t>(c0 + j) * e.out_ld[o] + r, e.out_type[o], v[j]);
             }
         }
+        return;
     }
-    __syncwarp();
+    // Muon update W = decay*W - lr*s*v in W's own orientation (x holds W)
+    float* w = x;
+#pragma unroll
+    for (int j = 0; j < CH; ++j) w[j] = fmaf(-e.lrs, v[j], e.decay * x[j]);
+    if (!e.transposed) {
+        const int64_t rb = static_cast<int64_t>(r) * e.w_cols;
+        if (full && e.w_vec) {
+#pragma unroll
+            for (int j = 0; j < CH; j += 8) st8(e.w, rb + c0 + j, e.w_type, w + j);
+        } else {
+#pragma unroll
+            for (int j = 0; j < CH; ++j)
+                if (j < ncol) store_elem(e.w, rb + c0 + j, e.w_type, w[j]);
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < CH; ++j)
+            if (j < ncol) store_elem(e.w, static_cast<int64_t>(c0 + j) * e.w_cols + r, e.w_type, w[j]);
+    }
 }
 
 __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_constant__ LaunchList L) {
@@ -329,7 +431,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&S.acc_full[b], 1);
-            mbar_init(&S.acc_empty[b], 4 * 32);
+            mbar_init(&S.acc_empty[b], kTcThreads - 64);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -428,27 +530,40 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
         }
     } else if (warp >= 2) {
         // ------------------------------------------------ epilogue
-        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        const int q = warp & 3;             // TMEM lane quarter this warp may access
+        const int half = (warp - 2) / 4;    // which 128 of the 256 columns
         int it = 0;
         for (int t = blockIdx.x; t < L.total_tiles; t += gridDim.x, ++it) {
             const TileCoord tc = decode_tile(L, t);
             const GemmGroup& g = L.groups[L.idx[tc.gi]];
             const int buf = it & 1;
             const uint32_t use = static_cast<uint32_t>(it >> 1);
+            const EpiRegs e = load_epi(g, L, tc.mat);
+            const int r = tc.tm * BM + q * 32 + lane;
+            const int row_last = tc.tm * BM + BM - 1;
+            // chunks of this warp that hold stored columns
+            constexpr int kChunks = (BN / 2) / CH;
+            const int ch0 = half * kChunks;
+            int nch = 0;
+            for (int ch = ch0; ch < ch0 + kChunks; ++ch) {
+                const int c0 = tc.tn * BN + ch * CH;
+                if (c0 >= e.N || (e.sym && e.mode == EPI_STORE && c0 > row_last)) break;
+                ++nch;
+            }
+            float xin[CH];
+            if (nch > 0) epi_load(e, r, tc.tn * BN + ch0 * CH, xin);
             if (!mbar_wait(&S.acc_full[buf], use & 1, L.status)) break;
             tc_fence_after();
-            const EpiRegs e = load_epi(g, L, tc.mat);
-            const int r0 = tc.tm * BM + q * 32;
-            const int row_last = tc.tm * BM + BM - 1;
-            float* st = S.stage[warp - 2];
-            for (int ch = 0; ch < BN / 32; ++ch) {
-                const int c0 = tc.tn * BN + ch * 32;
-                if (c0 >= e.N) break;
-                if (e.sym && e.mode == EPI_STORE && c0 > row_last) break;
-                float v[32];
+            for (int k = 0; k < nch; ++k) {
+                const int c0 = tc.tn * BN + (ch0 + k) * CH;
+                float x[CH];
+#pragma unroll
+                for (int j = 0; j < CH; ++j) x[j] = xin[j];
+                if (k + 1 < nch) epi_load(e, r, c0 + CH, xin);
+                float v[CH];
                 __syncwarp();
-                tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN + ch * 32), v);
-                if (r0 < e.M) epi_chunk(e, st, r0, c0, lane, v);
+                tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN + (ch0 + k) * CH), v);
+                epi_finish(e, r, c0, v, x);
             }
             __syncwarp();
             tc_fence_before();
