@@ -219,6 +219,33 @@ const char* dmuon_status_string(int status);
 int dmuon_debug_buffer(dmuon_handle_t h, int64_t wave, int64_t piece, int32_t which,
                        uint64_t* offset, int64_t* ld, int64_t* batch_stride);
 
+/* ---- one small matrix without device allocation ------------------------
+ *
+ * No counterpart in the paper: an addition for callers that cannot allocate
+ * device memory, so cannot give dmuon_step its workspace -- code whose device
+ * memory is entirely held by another allocator (a framework's caching pool),
+ * or that runs under a fixed memory budget and may not grow device
+ * allocations once training started.
+ *
+ * One Muon step (formula in the file header; defaults only: quintic
+ * (3.4445, -4.7750, 2.0315), eps 1e-7, Nesterov, aspect scale) on ONE matrix,
+ * in fp32 FFMA arithmetic (the numerics of DMUON_PREC_FP32), in one thread
+ * block on `stream`.  param and momentum (device, rows x cols, row-major,
+ * dtype DMUON_BF16 | DMUON_FP32, 16-byte aligned) are updated in place; grad
+ * is read.  Its scratch is a static device array of 1.3125 MiB that every GPU
+ * loading the library holds until exit, which limits the shape to
+ * min(rows, cols) <= 128 and rows*cols <= 262144; larger shapes return
+ * DMUON_ERR_INVALID_ARG with the limit in dmuon_last_error().  It calls no
+ * cudaMalloc, cudaFree or other allocating routine.  The first call on a
+ * device looks up the array's device address (cudaGetSymbolAddress, with
+ * that device current); make that first call before any stream capture.
+ * All calls on a device share the array: calls that may overlap on the GPU
+ * (unordered streams) race on it and must be serialised by the caller.
+ * Returns DMUON_OK, DMUON_ERR_INVALID_ARG, DMUON_ERR_ALIGN,
+ * DMUON_ERR_UNSUPPORTED_DTYPE or DMUON_ERR_CUDA. */
+int dmuon_step_noalloc(void* param, const void* grad, void* momentum, int64_t rows, int64_t cols,
+                       int32_t dtype, float lr, float beta, float wd, int32_t ns_steps, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -62,6 +62,8 @@ SIGNATURES = {
     "dmuon_status_string": (c_char_p, [c_int]),
     "dmuon_debug_buffer": (c_int, [c_void_p, c_int64, c_int64, c_int32, POINTER(c_uint64), POINTER(c_int64),
                                    POINTER(c_int64)]),
+    "dmuon_step_noalloc": (c_int, [c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_int32, c_float, c_float,
+                                   c_float, c_int32, c_void_p]),
 }
 
 _lib = None

@@ -268,6 +268,11 @@ std::vector<std::vector<int>> direct_sequence(int T) {
 
 }  // namespace
 
+namespace dmuon {
+// The calling thread's error message, also for the other translation units.
+void set_last_error(const std::string& msg) { g_last_error = msg; }
+}  // namespace dmuon
+
 static const std::vector<std::vector<Launch>>& launches_for(dmuon_plan_s* h, int T) {
     auto it = h->phase_cache.find(T);
     if (it != h->phase_cache.end()) return it->second;
