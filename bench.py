@@ -39,7 +39,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=3)
-    ap.add_argument("--budget-gb", type=float, default=0.0, help="workspace budget per wave (0 = one wave)")
+    ap.add_argument("--budget-gb", type=float, default=0.0,
+                    help="workspace budget per wave in GiB (0 = the configuration's own)")
     return ap.parse_args()
 
 
@@ -221,7 +222,7 @@ def run_dmuon(args, cfg, world, rank, local):
 
     _lib.load(build_if_missing=True)
     dt = 0 if cfg.dtype == "bf16" else 1
-    budget = int(args.budget_gb * (1 << 30))
+    budget = int((args.budget_gb or cfg.budget_gb) * (1 << 30))
     muon = Muon([(r, c, dt) for r, c in cfg.shapes], precision=cfg.precision, workspace_budget=budget).bind()
     ws, gs, ms = workloads.make_set(cfg, "cuda")
     torch.cuda.synchronize()

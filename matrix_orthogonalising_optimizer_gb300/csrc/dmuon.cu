@@ -170,12 +170,12 @@ int build_group(const GroupSpec& s, GemmGroup* g) {
         g->out_bs[o] = s.out[o].bs;
     }
     if (s.kernel == kKernelTc) {
-        g->tiles_m = static_cast<int32_t>((s.M + kTcBM - 1) / kTcBM);
+        // pair tiles: 256 rows (two CTAs of 128) x 256 columns
+        const int64_t pair_rows = kTcPair * kTcBM;
+        g->tiles_m = static_cast<int32_t>((s.M + pair_rows - 1) / pair_rows);
         g->tiles_n = static_cast<int32_t>((s.N + kTcBN - 1) / kTcBN);
         if (s.sym) {
-            int64_t t = 0;
-            for (int i = 0; i < g->tiles_m; ++i) t += std::min<int64_t>(i / 2 + 1, g->tiles_n);
-            g->tiles_per_mat = static_cast<int32_t>(t);
+            g->tiles_per_mat = g->tiles_m * (g->tiles_m + 1) / 2;
         } else {
             g->tiles_per_mat = g->tiles_m * g->tiles_n;
         }
@@ -184,7 +184,8 @@ int build_group(const GroupSpec& s, GemmGroup* g) {
         int rc = encode_bf16(&g->tma_a, s.a.p, s.K, s.M, s.batch, s.a.ld, s.a.bs, kTcSlabBytes / 2, kTcBM);
         if (rc) return rc;
         if (!s.b_mn)
-            rc = encode_bf16(&g->tma_b, s.b.p, s.K, s.N, s.batch, s.b.ld, s.b.bs, kTcSlabBytes / 2, kTcBN);
+            rc = encode_bf16(&g->tma_b, s.b.p, s.K, s.N, s.batch, s.b.ld, s.b.bs, kTcSlabBytes / 2,
+                             kTcBN / kTcPair);
         else
             rc = encode_bf16(&g->tma_b, s.b.p, s.N, s.K, s.batch, s.b.ld, s.b.bs, 64, kTcSlabBytes / 2);
         if (rc) return rc;

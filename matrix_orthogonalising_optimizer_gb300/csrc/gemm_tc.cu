@@ -9,9 +9,13 @@
 // group (bucket x product) of a phase, so small matrices share the machine
 // (section 2.2 "batching").
 //
-// Layout of one CTA (one per SM, persistent over a static round-robin tile
-// schedule):
+// Layout: clusters of two CTAs (one CTA per SM), persistent over a static
+// round-robin schedule of 256 x 256 pair tiles.  Each CTA of a pair computes
+// 128 rows; the pair shares the 256-column B tile, each CTA loading one half
+// with a TMA multicast into both, which cuts L2 reads per FLOP by a third.
+// Per CTA:
 //   warp 0      one thread issues TMA loads into a 4-stage shared-memory ring
+//               (a stage is free once both CTAs' MMAs have read it)
 //   warp 1      allocates 512 TMEM columns; one thread issues tcgen05.mma
 //               (kind::f16, bf16 operands, fp32 accumulation) into one of two
 //               128 x 256 fp32 accumulators
@@ -45,6 +49,8 @@ constexpr uint32_t STAGE_TX = A_BYTES + B_BYTES;
 constexpr uint32_t TMEM_COLS = 512;             // two 256-column accumulators
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr int CH = 16;                          // epilogue chunk: columns per tcgen05.ld
+constexpr int kPair = kTcPair;                   // CTAs per cluster sharing the B tile
+constexpr uint16_t kPairMask = (1u << kPair) - 1;
 
 struct __align__(1024) Smem {
     uint8_t a[STAGES][A_BYTES];
@@ -120,6 +126,40 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
         : "memory");
 }
 
+// Same, multicast: the box lands at the same shared-memory offset in every CTA
+// of the cluster named in `mask`, and each signals its own mbarrier there.
+__device__ __forceinline__ void tma_load_3d_mc(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1,
+                                               int c2, uint16_t mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(saddr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(saddr(bar)), "h"(mask)
+        : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_id() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t num_clusters() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+
+// All threads of both CTAs of the pair.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
 // A tensor map written by a host copy must be acquired by the tensormap proxy
 // before TMA reads it.
 __device__ __forceinline__ void tensormap_acquire(const CUtensorMap* map) {
@@ -162,6 +202,16 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
                  : "memory");
 }
 
+// Arrive on the mbarrier at this offset in every CTA of `mask` once this
+// thread's MMAs so far have completed.
+__device__ __forceinline__ void umma_commit_mc(uint64_t* bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            saddr(bar)),
+        "h"(mask)
+        : "memory");
+}
+
 // CH = 16 consecutive fp32 columns of this thread's TMEM lane.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[CH]) {
     uint32_t r[16];
@@ -180,9 +230,11 @@ struct TileCoord {
     int gi, mat, tm, tn;
 };
 
-// Static schedule: tile index -> (group, matrix, row tile, column tile).
-// Symmetric groups enumerate row tile i with column tiles 0 .. i/2 (a 256-wide
-// column tile covers two 128-high row tiles), i.e. the lower triangle.
+// Static schedule over pair tiles: index -> (group, matrix, pair row, column
+// tile).  A pair tile is 256 x 256; CTA rank r of the pair computes its rows
+// 128 r .. 128 r + 127 (a 128 x 256 accumulator), and the two share the B
+// tile.  Symmetric groups enumerate pair row i with column tiles 0 .. i, the
+// lower triangle.
 __device__ __forceinline__ TileCoord decode_tile(const LaunchList& L, int t) {
     TileCoord c;
     int gi = 0;
@@ -194,16 +246,16 @@ __device__ __forceinline__ TileCoord decode_tile(const LaunchList& L, int t) {
     int idx = local % g.tiles_per_mat;
     if (g.sym) {
         int i = 0;
-        while (idx >= i / 2 + 1) {
-            idx -= i / 2 + 1;
+        while (idx >= i + 1) {
+            idx -= i + 1;
             ++i;
         }
         c.tm = i;
         c.tn = idx;
     } else {
-        // Panels of kPanel column tiles, row tiles inside a panel: a wave of
-        // 152 CTAs then covers about 19 x 8 tiles, whose A rows and B columns
-        // stay in L2, instead of re-streaming all of B once per row of tiles.
+        // Panels of kPanel column tiles, pair rows inside a panel: a wave of
+        // 76 pairs then covers about 10 x 8 pair tiles, whose A rows and B
+        // columns stay in L2, instead of re-streaming all of B once per row.
         constexpr int kPanel = 8;
         const int panel_tiles = g.tiles_m * kPanel;
         const int panel = idx / panel_tiles;
@@ -328,6 +380,38 @@ __device__ __forceinline__ void load_row(const char* base, int32_t type, int32_t
     }
 }
 
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
+}
+
+// At tile start, a whole mainloop before use: pull into L2 every W / aux line
+// this thread's chunks will read (chunks c0, c0 + CH, ... of nch), so the
+// epilogue's loads hit L2 instead of HBM.  By-column inputs (transposed W,
+// symmetric aux) are row segments of 32 lanes, one line per input row.
+__device__ __forceinline__ void prefetch_rows(const char* base, int32_t type, int32_t ld, bool by_col, int r,
+                                              int r0, int lane, int c_first, int ncols, int M, int N) {
+    const int es = type == ELEM_BF16 ? 2 : 4;
+    if (!by_col) {
+        if (r >= M) return;
+        const int c_end = min(c_first + ncols, N);
+        for (int c = c_first; c < c_end; c += 128 / es)
+            prefetch_l2(base + (static_cast<int64_t>(r) * ld + c) * es);
+    } else {
+        if (r0 >= M) return;  // no valid row in this warp's 32 lanes
+        for (int c = c_first + lane; c < min(c_first + ncols, N); c += 32)
+            prefetch_l2(base + (static_cast<int64_t>(c) * ld + r0) * es);
+    }
+}
+
+__device__ __forceinline__ void epi_prefetch(const EpiRegs& e, int r, int r0, int lane, int c_first, int ncols) {
+    if (e.mode == EPI_UPDATE) {
+        prefetch_rows(e.w, e.w_type, e.w_cols, e.transposed, r, r0, lane, c_first, ncols, e.M, e.N);
+        if (e.aux) prefetch_rows(e.aux, e.aux_type, e.aux_ld, e.aux_sym, r, r0, lane, c_first, ncols, e.M, e.N);
+    } else if (e.aux) {
+        prefetch_rows(e.aux, e.aux_type, e.aux_ld, e.aux_sym, r, r0, lane, c_first, ncols, e.M, e.N);
+    }
+}
+
 // Prefetched input of a chunk: W for the update, else the aux operand.
 __device__ __forceinline__ void epi_load(const EpiRegs& e, int r, int c0, float (&x)[CH]) {
     if (r >= e.M || c0 >= e.N) return;
@@ -427,7 +511,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&S.full[s], 1);
-            mbar_init(&S.empty[s], 1);
+            mbar_init(&S.empty[s], kPair);  // both CTAs' MMAs release a stage
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&S.acc_full[b], 1);
@@ -443,8 +527,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     }
     tc_fence_before();
     __syncthreads();
+    cluster_sync();  // the partner's barriers exist before any multicast targets them
     tc_fence_after();
     const uint32_t tmem = S.tmem_base;
+    const int rank = static_cast<int>(cluster_rank());
+    const int pair0 = static_cast<int>(cluster_id());
+    const int npairs = static_cast<int>(num_clusters());
 
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------ TMA producer
@@ -455,7 +543,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
             tensormap_acquire(&L.groups[L.idx[j]].tma_a);
             tensormap_acquire(&L.groups[L.idx[j]].tma_b);
         }
-        for (int t = blockIdx.x; t < L.total_tiles && ok; t += gridDim.x) {
+        for (int t = pair0; t < L.total_tiles && ok; t += npairs) {
             const TileCoord tc = decode_tile(L, t);
             const GemmGroup* g = L.groups + L.idx[tc.gi];
             const int nkb = (g->K + SLAB_K - 1) / SLAB_K;
@@ -467,14 +555,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
                 mbar_expect_tx(&S.full[stage], STAGE_TX);
                 issued |= 1u << stage;
                 issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-                tma_load_3d(S.a[stage], &g->tma_a, &S.full[stage], kb * SLAB_K, tc.tm * BM, tc.mat);
+                // own 128 rows of A; own half of the shared B tile, multicast to
+                // both CTAs of the pair (the partner sends the other half)
+                tma_load_3d(S.a[stage], &g->tma_a, &S.full[stage], kb * SLAB_K, (2 * tc.tm + rank) * BM, tc.mat);
                 if (!g->b_mn_major) {
-                    tma_load_3d(S.b[stage], &g->tma_b, &S.full[stage], kb * SLAB_K, tc.tn * BN, tc.mat);
+                    tma_load_3d_mc(S.b[stage] + rank * (B_BYTES / kPair), &g->tma_b, &S.full[stage], kb * SLAB_K,
+                                   tc.tn * BN + rank * (BN / kPair), tc.mat, kPairMask);
                 } else {
 #pragma unroll
-                    for (int i = 0; i < BN / 64; ++i)
-                        tma_load_3d(S.b[stage] + i * MN_BOX_BYTES, &g->tma_b, &S.full[stage], tc.tn * BN + 64 * i,
-                                    kb * SLAB_K, tc.mat);
+                    for (int i = 0; i < BN / 64 / kPair; ++i) {
+                        const int box = rank * (BN / 64 / kPair) + i;
+                        tma_load_3d_mc(S.b[stage] + box * MN_BOX_BYTES, &g->tma_b, &S.full[stage],
+                                       tc.tn * BN + 64 * box, kb * SLAB_K, tc.mat, kPairMask);
+                    }
                 }
                 if (++stage == STAGES) {
                     stage = 0;
@@ -486,13 +579,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
             // let copies already issued land before the CTA can exit
             for (int s = 0; s < STAGES; ++s)
                 if (issued & (1u << s)) mbar_wait(&S.full[s], (issued_parity >> s) & 1u, L.status);
+        } else {
+            // wait for both MMAs' releases of the last ring round, so no
+            // arrival from the partner is still in flight towards this CTA
+            // when the pair leaves through the final cluster barrier
+            for (int i = 0; i < STAGES && ok; ++i) {
+                ok = mbar_wait(&S.empty[stage], phase ^ 1, L.status);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
         }
     } else if (warp == 1 && lane == 0) {
         // ------------------------------------------------ MMA issuer
         uint32_t stage = 0, phase = 0;
         bool ok = true;
         int it = 0;
-        for (int t = blockIdx.x; t < L.total_tiles && ok; t += gridDim.x, ++it) {
+        for (int t = pair0; t < L.total_tiles && ok; t += npairs, ++it) {
             const TileCoord tc = decode_tile(L, t);
             const GemmGroup* g = L.groups + L.idx[tc.gi];
             const int nkb = (g->K + SLAB_K - 1) / SLAB_K;
@@ -518,7 +622,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
                                             : smem_desc(b0 + kk * (UMMA_K * 2), 0, 1024);
                     umma_bf16(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
                 }
-                umma_commit(&S.empty[stage]);
+                umma_commit_mc(&S.empty[stage], kPairMask);
                 if (++stage == STAGES) {
                     stage = 0;
                     phase ^= 1;
@@ -533,14 +637,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
         const int q = warp & 3;             // TMEM lane quarter this warp may access
         const int half = (warp - 2) / 4;    // which 128 of the 256 columns
         int it = 0;
-        for (int t = blockIdx.x; t < L.total_tiles; t += gridDim.x, ++it) {
+        for (int t = pair0; t < L.total_tiles; t += npairs, ++it) {
             const TileCoord tc = decode_tile(L, t);
             const GemmGroup& g = L.groups[L.idx[tc.gi]];
             const int buf = it & 1;
             const uint32_t use = static_cast<uint32_t>(it >> 1);
             const EpiRegs e = load_epi(g, L, tc.mat);
-            const int r = tc.tm * BM + q * 32 + lane;
-            const int row_last = tc.tm * BM + BM - 1;
+            const int tm = 2 * tc.tm + rank;  // this CTA's 128-row tile
+            const int r = tm * BM + q * 32 + lane;
+            const int row_last = tm * BM + BM - 1;
             // chunks of this warp that hold stored columns
             constexpr int kChunks = (BN / 2) / CH;
             const int ch0 = half * kChunks;
@@ -550,6 +655,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
                 if (c0 >= e.N || (e.sym && e.mode == EPI_STORE && c0 > row_last)) break;
                 ++nch;
             }
+            if (nch > 0) epi_prefetch(e, r, tm * BM + q * 32, lane, tc.tn * BN + ch0 * CH, nch * CH);
             float xin[CH];
             if (nch > 0) epi_load(e, r, tc.tn * BN + ch0 * CH, xin);
             if (!mbar_wait(&S.acc_full[buf], use & 1, L.status)) break;
@@ -573,6 +679,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
 
     tc_fence_before();
     __syncthreads();
+    // neither CTA leaves while the partner may still multicast into its shared
+    // memory or arrive on its barriers
+    cluster_sync();
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
@@ -586,17 +695,32 @@ size_t gemm_tc_smem_bytes() { return sizeof(Smem) + 1024; }
 
 cudaError_t launch_gemm_tc(const LaunchList& l, int num_sms, cudaStream_t s) {
     if (l.total_tiles <= 0) return cudaSuccess;
-    static bool attr_set = false;
+    static int max_pairs = 0;
     const size_t smem = gemm_tc_smem_bytes();
-    if (!attr_set) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kPair;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (max_pairs == 0) {
         cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
         if (e != cudaSuccess) return e;
-        attr_set = true;
+        cfg.gridDim = dim3(num_sms / kPair * kPair);
+        int n = 0;
+        e = cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel, &cfg);
+        if (e != cudaSuccess) return e;
+        max_pairs = n > 0 ? n : num_sms / kPair;
     }
-    const int grid = l.total_tiles < num_sms ? l.total_tiles : num_sms;
-    gemm_tc_kernel<<<grid, kTcThreads, smem, s>>>(l);
-    return cudaGetLastError();
+    const int pairs = l.total_tiles < max_pairs ? l.total_tiles : max_pairs;
+    cfg.gridDim = dim3(pairs * kPair);
+    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, l);
 }
 
 }  // namespace dmuon

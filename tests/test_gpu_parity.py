@@ -234,3 +234,54 @@ def test_c4_heterogeneous_sampled():
     want = oracle_O([inputs[i] for i in picks], beta=BETA)
     errs = [rel_fro(got[i], w) for i, w in zip(picks, want)]
     assert max(errs) <= 3e-2, max(errs)
+
+
+# ------------------------------------------------------------------ full-size sets, sampled
+
+
+def _full_size_sampled(name, picks):
+    """Whole set generated on the GPU and stepped in bench.py's launch
+    configuration (W = 0, lr = 1, wd = 0); sampled matrices checked against the
+    oracle one by one on the host."""
+    import gc
+
+    from matrix_orthogonalising_optimizer_gb300 import Muon
+    cfg = workloads.get(name)
+    gc.collect()
+    torch.cuda.empty_cache()
+    muon = Muon([(r, c, 0) for r, c in cfg.shapes], workspace_budget=int(cfg.budget_gb * (1 << 30))).bind()
+    ws, gs, ms = workloads.make_set(cfg, "cuda")
+    for w in ws:
+        w.zero_()
+    muon.step(ws, gs, ms, 1.0, BETA, 0.0, cfg.ns_steps)
+    torch.cuda.synchronize()
+    assert muon.device_status() == 0
+    errs = {}
+    for i in picks:
+        r, c = cfg.shapes[i]
+        g = gs[i].cpu()
+        o_gpu = -ws[i].double().cpu().numpy() / oracle.shape_scale(r, c)
+        # momenta were zero: M' = grad bitwise
+        assert torch.equal(ms[i].cpu(), g)
+        want = oracle.muon_step(np.zeros((r, c)), g.double().numpy(), np.zeros((r, c)), lr=1.0, beta=BETA,
+                                wd=0.0, ns_steps=cfg.ns_steps)["O"]
+        errs[(i, r, c)] = rel_fro(o_gpu, want)
+    del ws, gs, ms, muon
+    gc.collect()
+    torch.cuda.empty_cache()
+    assert max(errs.values()) <= 3e-2, errs
+    return errs
+
+
+def test_c3_llama_full_size_sampled():
+    # one matrix per bucket: k (1024x4096, Gram), q (4096^2, direct), gate (14336x4096, tall, Gram),
+    # down (4096x14336, wide, Gram)
+    _full_size_sampled("c3", [1, 0, 4, 6])
+
+
+def test_c5_large_layers_full_size_sampled():
+    free, total = torch.cuda.mem_get_info()
+    if free < 280e9:
+        pytest.skip(f"needs about 280 GB free, {free / 1e9:.0f} GB free")
+    # 8192^2 (direct) and 28672x8192 (tall, Gram)
+    _full_size_sampled("c5", [0, 1])

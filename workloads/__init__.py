@@ -43,6 +43,7 @@ class Config:
     ns_steps: int = 5
     precision: str = "bf16"     # 'bf16' | 'fp32'
     logscale: tuple = field(default=(0.0, 0.0))   # per-matrix 10**U(lo, hi)
+    budget_gb: float = 0.0      # workspace per wave (0 = the whole set in one wave)
 
 
 def _layers(n, per_layer):
@@ -75,7 +76,7 @@ CONFIGS = {
                  _vla_shapes(3), "logscale", logscale=(-5.0, -1.0)),
     "c5": Config("c5", "large-layer stress, 80 x {8192x8192, 28672x8192, 8192x28672}", "bf16", 4,
                  _layers(80, ((8192, 8192), (28672, 8192), (8192, 28672))), "normal",
-                 grad_scale=1e-3),
+                 grad_scale=1e-3, budget_gb=16.0),
 }
 
 
