@@ -327,6 +327,8 @@ static const std::vector<std::vector<Launch>>& launches_for(dmuon_plan_s* h, int
                     l.scalars = reinterpret_cast<const SlotScalars*>(ws + h->off_scalars);
                     l.params = reinterpret_cast<void* const*>(ws + h->off_ptrs);
                     l.status = reinterpret_cast<int32_t*>(ws + h->off_status);
+                    if (launches.size() < static_cast<size_t>(kMaxLaunchesPerWave))
+                        l.counter = reinterpret_cast<int32_t*>(ws + h->off_counters) + launches.size();
                     launches.push_back(la);
                 }
             }
@@ -526,7 +528,8 @@ dmuon_handle_t dmuon_plan_ex(const dmuon_shape_t* shapes, int64_t count, const d
     h->off_infos = h->off_scalars + up(nslots * sizeof(SlotScalars), 256);
     h->off_ptrs = h->off_infos + up(nslots * sizeof(MatInfo), 256);
     h->off_groups = h->off_ptrs + up(3 * static_cast<uint64_t>(count) * sizeof(void*), 256);
-    h->off_waves = h->off_groups + up(static_cast<uint64_t>(ngroups) * sizeof(GemmGroup), 256);
+    h->off_counters = h->off_groups + up(static_cast<uint64_t>(ngroups) * sizeof(GemmGroup), 256);
+    h->off_waves = h->off_counters + up(kMaxLaunchesPerWave * sizeof(int32_t), 256);
     h->ws_bytes = h->off_waves + max_wave;
     return h;
 }
@@ -893,6 +896,11 @@ int dmuon_step(dmuon_handle_t h, void* const* params, const void* const* grads, 
         cudaError_t e = timed(h, s, DMUON_TIMER_MOMENTUM, -1, [&] { return launch_momentum_pack(ma, s); });
         if (e == cudaSuccess) e = timed(h, s, DMUON_TIMER_NORM, -1, [&] { return launch_norm_finalize(ma, s); });
         if (e != cudaSuccess) return fail(DMUON_ERR_CUDA, std::string("momentum launch: ") + cudaGetErrorString(e));
+        if (per_wave[wi].size() > static_cast<size_t>(kMaxLaunchesPerWave))
+            return fail(DMUON_ERR_INVALID_ARG, "too many launches in one wave");
+        // the tensor-core launches take tiles from per-launch counters
+        e = cudaMemsetAsync(h->ws + h->off_counters, 0, per_wave[wi].size() * sizeof(int32_t), s);
+        if (e != cudaSuccess) return fail(DMUON_ERR_CUDA, std::string("counter reset: ") + cudaGetErrorString(e));
         for (const Launch& la : per_wave[wi]) {
             LaunchList l = la.list;
             l.lr = lr;

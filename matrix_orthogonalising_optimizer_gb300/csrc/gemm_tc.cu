@@ -9,8 +9,8 @@
 // group (bucket x product) of a phase, so small matrices share the machine
 // (section 2.2 "batching").
 //
-// Layout: clusters of two CTAs (one CTA per SM), persistent over a static
-// round-robin schedule of 256 x 256 pair tiles.  Each CTA of a pair computes
+// Layout: clusters of two CTAs (one CTA per SM), persistent over a dynamic
+// schedule of 256 x 256 pair tiles taken in order from a per-launch counter.  Each CTA of a pair computes
 // 128 rows; the pair shares the 256-column B tile, each CTA loading one half
 // with a TMA multicast into both, which cuts L2 reads per FLOP by a third.
 // Per CTA:
@@ -48,6 +48,10 @@ constexpr int MN_BOX_BYTES = SLAB_K * 128;      // one MN-major box: 64 K-rows x
 constexpr uint32_t STAGE_TX = A_BYTES + B_BYTES;
 constexpr uint32_t TMEM_COLS = 512;             // two 256-column accumulators
 constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr int kTileRing = 4;
+// readers of a tile slot: per CTA the MMA thread and the 8 epilogue warps,
+// plus the partner's producer
+constexpr uint32_t kTileReaders = 2 * (1 + (kTcThreads - 64) / 32) + 1;
 constexpr int CH = 16;                          // epilogue chunk: columns per tcgen05.ld
 constexpr int kPair = kTcPair;                   // CTAs per cluster sharing the B tile
 constexpr uint16_t kPairMask = (1u << kPair) - 1;
@@ -59,6 +63,9 @@ struct __align__(1024) Smem {
     uint64_t empty[STAGES];
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
+    uint64_t tile_full[kTileRing];   // a tile index is in tile_slot (count 1)
+    uint64_t tile_empty[kTileRing];  // leader only: every reader of both CTAs is done
+    int32_t tile_slot[kTileRing];
     uint32_t tmem_base;
 };
 
@@ -143,16 +150,47 @@ __device__ __forceinline__ uint32_t cluster_rank() {
     return r;
 }
 
-__device__ __forceinline__ uint32_t cluster_id() {
+// Shared::cluster address of the same variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
     uint32_t r;
-    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
     return r;
 }
 
-__device__ __forceinline__ uint32_t num_clusters() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
-    return r;
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr, int32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// Arrive (release, cluster scope) on an mbarrier of this or the partner CTA.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(saddr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait with cluster-scope acquire (the arrivals come from the partner).
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, int32_t* status) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 256; ++i)
+            if (mbar_try_wait_cluster(bar, parity)) return true;
+        if (globaltimer() - t0 > kWaitNs) {
+            atomicExch(status, DEV_TIMEOUT);
+            return false;
+        }
+    }
 }
 
 // All threads of both CTAs of the pair.
@@ -229,6 +267,25 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[CH]) {
 struct TileCoord {
     int gi, mat, tm, tn;
 };
+
+// Dynamic schedule.  The pair's leader producer takes pair tiles from the
+// launch's counter in order and publishes each index in a ring slot of both
+// CTAs; readers wait for the slot, read it, and release it to the leader.
+// Taking tiles in order keeps the pairs working on neighbouring tiles, whose
+// operands are shared in L2 (a static round-robin lets the pairs drift apart
+// over a long launch and thrash L2).  Returns the tile index, or a value
+// >= total_tiles when the launch is out of tiles or a wait timed out.
+__device__ __forceinline__ int wait_tile(uint64_t* full, const int32_t* slots, int k, int32_t* status, int total) {
+    const int slot = k % kTileRing;
+    const uint32_t ph = static_cast<uint32_t>(k / kTileRing) & 1u;
+    if (!mbar_wait_cluster(&full[slot], ph, status)) return total;
+    return *reinterpret_cast<const volatile int32_t*>(&slots[slot]);
+}
+
+// After every thread of the reader has read slot k: give it back to the leader.
+__device__ __forceinline__ void release_tile(uint64_t* empty, int k) {
+    mbar_arrive_cluster(mapa(saddr(&empty[k % kTileRing]), 0));
+}
 
 // Static schedule over pair tiles: index -> (group, matrix, pair row, column
 // tile).  A pair tile is 256 x 256; CTA rank r of the pair computes its rows
@@ -517,6 +574,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
             mbar_init(&S.acc_full[b], 1);
             mbar_init(&S.acc_empty[b], kTcThreads - 64);
         }
+        for (int i = 0; i < kTileRing; ++i) {
+            mbar_init(&S.tile_full[i], 1);
+            mbar_init(&S.tile_empty[i], kTileReaders);
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
@@ -531,8 +592,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     tc_fence_after();
     const uint32_t tmem = S.tmem_base;
     const int rank = static_cast<int>(cluster_rank());
-    const int pair0 = static_cast<int>(cluster_id());
-    const int npairs = static_cast<int>(num_clusters());
+    const int total = L.total_tiles;
 
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------ TMA producer
@@ -543,7 +603,27 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
             tensormap_acquire(&L.groups[L.idx[j]].tma_a);
             tensormap_acquire(&L.groups[L.idx[j]].tma_b);
         }
-        for (int t = pair0; t < L.total_tiles && ok; t += npairs) {
+        for (int k = 0; ok; ++k) {
+            int t;
+            if (rank == 0) {
+                // take the next tile and publish it in both CTAs' ring slot
+                const int slot = k % kTileRing;
+                const uint32_t ph = static_cast<uint32_t>(k / kTileRing) & 1u;
+                if (!mbar_wait_cluster(&S.tile_empty[slot], ph ^ 1u, L.status)) {
+                    ok = false;
+                    break;
+                }
+                t = atomicAdd(L.counter, 1);
+                if (t > total) t = total;
+                S.tile_slot[slot] = t;
+                st_cluster_u32(mapa(saddr(&S.tile_slot[slot]), 1), t);
+                mbar_arrive_cluster(mapa(saddr(&S.tile_full[slot]), 0));
+                mbar_arrive_cluster(mapa(saddr(&S.tile_full[slot]), 1));
+            } else {
+                t = wait_tile(S.tile_full, S.tile_slot, k, L.status, total);
+                release_tile(S.tile_empty, k);
+            }
+            if (t >= total) break;
             const TileCoord tc = decode_tile(L, t);
             const GemmGroup* g = L.groups + L.idx[tc.gi];
             const int nkb = (g->K + SLAB_K - 1) / SLAB_K;
@@ -596,7 +676,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
         uint32_t stage = 0, phase = 0;
         bool ok = true;
         int it = 0;
-        for (int t = pair0; t < L.total_tiles && ok; t += npairs, ++it) {
+        for (int k = 0; ok; ++k, ++it) {
+            const int t = wait_tile(S.tile_full, S.tile_slot, k, L.status, total);
+            release_tile(S.tile_empty, k);
+            if (t >= total) break;
             const TileCoord tc = decode_tile(L, t);
             const GemmGroup* g = L.groups + L.idx[tc.gi];
             const int nkb = (g->K + SLAB_K - 1) / SLAB_K;
@@ -637,7 +720,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
         const int q = warp & 3;             // TMEM lane quarter this warp may access
         const int half = (warp - 2) / 4;    // which 128 of the 256 columns
         int it = 0;
-        for (int t = pair0; t < L.total_tiles; t += npairs, ++it) {
+        for (int k = 0;; ++k, ++it) {
+            const int t = wait_tile(S.tile_full, S.tile_slot, k, L.status, total);
+            __syncwarp();
+            if (lane == 0) release_tile(S.tile_empty, k);
+            if (t >= total) break;
             const TileCoord tc = decode_tile(L, t);
             const GemmGroup& g = L.groups[L.idx[tc.gi]];
             const int buf = it & 1;
@@ -660,15 +747,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
             if (nch > 0) epi_load(e, r, tc.tn * BN + ch0 * CH, xin);
             if (!mbar_wait(&S.acc_full[buf], use & 1, L.status)) break;
             tc_fence_after();
-            for (int k = 0; k < nch; ++k) {
-                const int c0 = tc.tn * BN + (ch0 + k) * CH;
+            for (int kc = 0; kc < nch; ++kc) {
+                const int c0 = tc.tn * BN + (ch0 + kc) * CH;
                 float x[CH];
 #pragma unroll
                 for (int j = 0; j < CH; ++j) x[j] = xin[j];
-                if (k + 1 < nch) epi_load(e, r, c0 + CH, xin);
+                if (kc + 1 < nch) epi_load(e, r, c0 + CH, xin);
                 float v[CH];
                 __syncwarp();
-                tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN + (ch0 + k) * CH), v);
+                tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN + (ch0 + kc) * CH), v);
                 epi_finish(e, r, c0, v, x);
             }
             __syncwarp();

@@ -28,6 +28,7 @@ constexpr int kMomTile = 64;
 constexpr int kMomThreads = 256;
 
 constexpr int kMaxGroupsPerLaunch = 96;
+constexpr int kMaxLaunchesPerWave = 1024;  // tile counters in the workspace, cleared per wave
 
 enum ElemType : int32_t { ELEM_BF16 = 0, ELEM_F32 = 1 };
 enum EpiMode : int32_t { EPI_STORE = 0, EPI_UPDATE = 1 };
@@ -99,6 +100,7 @@ struct LaunchList {
     const SlotScalars* scalars;              // device, indexed by slot
     void* const* params;                     // device, indexed by gidx
     int32_t* status;                         // device status word
+    int32_t* counter;                        // tile counter of this launch (zero at launch)
     float lr, decay;                         // update: W = decay*W - lr*s*v
     int32_t n;                               // groups in this launch
     int32_t total_tiles;

@@ -89,7 +89,8 @@ struct dmuon_plan_s {
     std::vector<dmuon::SlotHost> slots;  // bucket order
 
     // fixed region layout
-    uint64_t off_status = 0, off_scalars = 0, off_infos = 0, off_ptrs = 0, off_groups = 0, off_waves = 0;
+    uint64_t off_status = 0, off_scalars = 0, off_infos = 0, off_ptrs = 0, off_groups = 0, off_counters = 0,
+             off_waves = 0;
     int64_t num_groups = 0;
     uint64_t ws_bytes = 0;
 
