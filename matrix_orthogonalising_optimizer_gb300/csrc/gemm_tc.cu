@@ -49,6 +49,7 @@ constexpr uint32_t STAGE_TX = A_BYTES + B_BYTES;
 constexpr uint32_t TMEM_COLS = 512;             // two 256-column accumulators
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr int kTileRing = 4;
+constexpr int kTStageLd = 132;  // 128 W columns + 4 pad; 528-byte rows keep float4 reads aligned
 // readers of a tile slot: per CTA the MMA thread and the 8 epilogue warps,
 // plus the partner's producer
 constexpr uint32_t kTileReaders = 2 * (1 + (kTcThreads - 64) / 32) + 1;
@@ -67,6 +68,9 @@ struct __align__(1024) Smem {
     uint64_t tile_empty[kTileRing];  // leader only: every reader of both CTAs is done
     int32_t tile_slot[kTileRing];
     uint32_t tmem_base;
+    // transposed W update: a 16 x 128 chunk of v per column half, padded rows
+    // (read as float4: 16-byte aligned)
+    alignas(16) float tstage[2][CH * kTStageLd];
 };
 
 __device__ __forceinline__ uint32_t saddr(const void* p) {
@@ -559,6 +563,86 @@ __device__ __forceinline__ void epi_finish(const EpiRegs& e, int r, int c0, floa
     }
 }
 
+// Transposed W update (tall matrices: D row r is W column r).  The four warps
+// of a column half own 32 D rows each, so alone each could touch only 64 bytes
+// of a W row at a time.  Instead they stage a 16 x 128 chunk of v in shared
+// memory and each warp then updates 4 whole W row segments of 128 columns,
+// 4 consecutive elements per lane (8- or 16-byte accesses).
+__device__ __forceinline__ void named_bar(int id) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(128) : "memory");
+}
+
+// Named barrier of the 128 threads of a column half that also returns the AND
+// of their predicates: the four warps take every loop exit together, so none
+// is left waiting at a barrier the others no longer reach.
+__device__ __forceinline__ bool named_bar_and(int id, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.and.pred p, %2, %3, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"(pred ? 1u : 0u), "r"(id), "r"(128)
+        : "memory");
+    return r != 0;
+}
+
+// W[c0 + 4q + i][wc .. wc+3] for i < 4 into w (rows beyond N, columns beyond M skipped).
+__device__ __forceinline__ void tw_load(const EpiRegs& e, int c0, int q, int wc, float (&w)[4][4]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int c = c0 + 4 * q + i;
+        if (c >= e.N) continue;
+        const int64_t base = static_cast<int64_t>(c) * e.w_cols + wc;
+        if (wc + 3 < e.M) {
+            if (e.w_type == ELEM_BF16) {
+                const uint2 u = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(e.w) + base);
+                const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+                const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+                w[i][0] = f0.x; w[i][1] = f0.y; w[i][2] = f1.x; w[i][3] = f1.y;
+            } else {
+                const float4 f = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(e.w) + base);
+                w[i][0] = f.x; w[i][1] = f.y; w[i][2] = f.z; w[i][3] = f.w;
+            }
+        } else {
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+                if (wc + t < e.M) w[i][t] = load_elem(e.w, base + t, e.w_type);
+        }
+    }
+}
+
+__device__ __forceinline__ void tw_store(const EpiRegs& e, int c0, int q, int wc, const float* stg, int lane,
+                                         const float (&w)[4][4]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int c = c0 + 4 * q + i;
+        if (c >= e.N) continue;
+        const float4 v = *reinterpret_cast<const float4*>(stg + (4 * q + i) * kTStageLd + 4 * lane);
+        const float n0 = fmaf(-e.lrs, v.x, e.decay * w[i][0]);
+        const float n1 = fmaf(-e.lrs, v.y, e.decay * w[i][1]);
+        const float n2 = fmaf(-e.lrs, v.z, e.decay * w[i][2]);
+        const float n3 = fmaf(-e.lrs, v.w, e.decay * w[i][3]);
+        const int64_t base = static_cast<int64_t>(c) * e.w_cols + wc;
+        if (wc + 3 < e.M) {
+            if (e.w_type == ELEM_BF16) {
+                uint2 u;
+                *reinterpret_cast<__nv_bfloat162*>(&u.x) = __floats2bfloat162_rn(n0, n1);
+                *reinterpret_cast<__nv_bfloat162*>(&u.y) = __floats2bfloat162_rn(n2, n3);
+                *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(e.w) + base) = u;
+            } else {
+                *reinterpret_cast<float4*>(reinterpret_cast<float*>(e.w) + base) = make_float4(n0, n1, n2, n3);
+            }
+        } else {
+            const float n[4] = {n0, n1, n2, n3};
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+                if (wc + t < e.M) store_elem(e.w, base + t, e.w_type, n[t]);
+        }
+    }
+}
+
 __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_constant__ LaunchList L) {
     extern __shared__ uint8_t smem_raw[];
     Smem& S = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -724,7 +808,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
             const int t = wait_tile(S.tile_full, S.tile_slot, k, L.status, total);
             __syncwarp();
             if (lane == 0) release_tile(S.tile_empty, k);
-            if (t >= total) break;
+            if (!named_bar_and(1 + half, t < total)) break;
             const TileCoord tc = decode_tile(L, t);
             const GemmGroup& g = L.groups[L.idx[tc.gi]];
             const int buf = it & 1;
@@ -743,6 +827,36 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
                 ++nch;
             }
             if (nch > 0) epi_prefetch(e, r, tm * BM + q * 32, lane, tc.tn * BN + ch0 * CH, nch * CH);
+            // tall matrices' update through the staged path (the same four warps
+            // of this half always see the same nch, so the named barriers match)
+            const bool tpath = e.mode == EPI_UPDATE && e.transposed && !e.aux && (e.w_cols % 4) == 0;
+            if (tpath) {
+                const int wc = tm * BM + 4 * lane;
+                float* stg = S.tstage[half];
+                float wn[4][4];
+                if (nch > 0) tw_load(e, tc.tn * BN + ch0 * CH, q, wc, wn);
+                const bool ready = mbar_wait(&S.acc_full[buf], use & 1, L.status);
+                if (!named_bar_and(1 + half, ready)) break;
+                tc_fence_after();
+                for (int kc = 0; kc < nch; ++kc) {
+                    const int c0 = tc.tn * BN + (ch0 + kc) * CH;
+                    float wcur[4][4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+#pragma unroll
+                        for (int t = 0; t < 4; ++t) wcur[i][t] = wn[i][t];
+                    if (kc + 1 < nch) tw_load(e, c0 + CH, q, wc, wn);
+                    float v[CH];
+                    __syncwarp();
+                    tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) +
+                                  static_cast<uint32_t>(buf * BN + (ch0 + kc) * CH), v);
+#pragma unroll
+                    for (int j = 0; j < CH; ++j) stg[j * kTStageLd + q * 32 + lane] = epi_v(e, r, c0 + j, v[j], 0.0f);
+                    named_bar(1 + half);
+                    tw_store(e, c0, q, wc, stg, lane, wcur);
+                    named_bar(1 + half);  // the chunk is read before the next one is staged
+                }
+            } else {
             float xin[CH];
             if (nch > 0) epi_load(e, r, tc.tn * BN + ch0 * CH, xin);
             if (!mbar_wait(&S.acc_full[buf], use & 1, L.status)) break;
@@ -757,6 +871,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
                 __syncwarp();
                 tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN + (ch0 + kc) * CH), v);
                 epi_finish(e, r, c0, v, x);
+            }
             }
             __syncwarp();
             tc_fence_before();
