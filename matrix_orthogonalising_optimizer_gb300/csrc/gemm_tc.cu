@@ -687,18 +687,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
             tensormap_acquire(&L.groups[L.idx[j]].tma_a);
             tensormap_acquire(&L.groups[L.idx[j]].tma_b);
         }
+        // the leader takes tile indices one ahead, so the atomic's latency
+        // hides behind the current tile's loads
+        int t_next = rank == 0 ? atomicAdd(L.counter, 1) : 0;
         for (int k = 0; ok; ++k) {
             int t;
             if (rank == 0) {
-                // take the next tile and publish it in both CTAs' ring slot
+                // publish the next tile in both CTAs' ring slot
                 const int slot = k % kTileRing;
                 const uint32_t ph = static_cast<uint32_t>(k / kTileRing) & 1u;
                 if (!mbar_wait_cluster(&S.tile_empty[slot], ph ^ 1u, L.status)) {
                     ok = false;
                     break;
                 }
-                t = atomicAdd(L.counter, 1);
-                if (t > total) t = total;
+                t = t_next < total ? t_next : total;
+                if (t < total) t_next = atomicAdd(L.counter, 1);
                 S.tile_slot[slot] = t;
                 st_cluster_u32(mapa(saddr(&S.tile_slot[slot]), 1), t);
                 mbar_arrive_cluster(mapa(saddr(&S.tile_full[slot]), 0));
