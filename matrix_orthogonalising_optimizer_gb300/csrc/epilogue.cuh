@@ -66,46 +66,82 @@ __device__ __forceinline__ EpiCtx make_epi_ctx(const GemmGroup& g, const LaunchL
     return c;
 }
 
-__device__ __forceinline__ float epi_aux(const GemmGroup& g, const EpiCtx& c, int r, int col) {
-    if (!c.aux) return 0.0f;
-    const int64_t i = g.aux_sym ? static_cast<int64_t>(col) * g.aux_ld + r
-                                : static_cast<int64_t>(r) * g.aux_ld + col;
-    return load_elem(c.aux, i, g.aux_type);
-}
+// Epilogue parameters of one tile, held in registers (the group table lives in
+// global memory, and stores through generic pointers would otherwise force
+// the compiler to reload every field after each store).
+struct EpiRegs {
+    const char* aux;
+    char* out[3];
+    char* w;
+    float alpha, c_acc, c_diag, c_aux, lrs, decay;
+    int32_t M, N, mode, sym, aux_type, aux_sym, aux_ld, w_type, w_cols, transposed, w_vec;
+    int32_t out_ld[3], out_type[3];
+};
 
-// The one per-element formula; every path computes it in this order.
-__device__ __forceinline__ float epi_value(const GemmGroup& g, const EpiCtx& c, int r, int col,
-                                           float acc, float aux) {
-    float t = g.c_acc * acc;
-    if (r == col) t += g.c_diag;
-    if (c.aux) t = fmaf(g.c_aux, aux, t);
-    return c.alpha * t;
-}
-
-__device__ __forceinline__ void epi_write(const GemmGroup& g, const EpiCtx& c, int i, int j, float v) {
+__device__ __forceinline__ EpiRegs load_epi(const GemmGroup& g, const LaunchList& L, int mat) {
+    const EpiCtx c = make_epi_ctx(g, L, mat);
+    EpiRegs e;
+    e.aux = static_cast<const char*>(c.aux);
 #pragma unroll
-    for (int o = 0; o < 3; ++o)
-        if (c.out[o]) store_elem(c.out[o], static_cast<int64_t>(i) * g.out_ld[o] + j, g.out_type[o], v);
+    for (int o = 0; o < 3; ++o) {
+        e.out[o] = static_cast<char*>(c.out[o]);
+        e.out_ld[o] = g.out_ld[o];
+        e.out_type[o] = g.out_type[o];
+    }
+    e.w = static_cast<char*>(c.w);
+    e.alpha = c.alpha;
+    e.c_acc = g.c_acc;
+    e.c_diag = g.c_diag;
+    e.c_aux = g.c_aux;
+    e.lrs = c.lrs;
+    e.decay = L.decay;
+    e.M = g.M;
+    e.N = g.N;
+    e.mode = g.mode;
+    e.sym = g.sym;
+    e.aux_type = g.aux_type;
+    e.aux_sym = g.aux_sym;
+    e.aux_ld = g.aux_ld;
+    e.w_type = c.w_type;
+    e.w_cols = c.w_cols;
+    e.transposed = c.transposed;
+    // 16-byte row access to W needs every row start on 16 bytes
+    e.w_vec = c.w && ((static_cast<int64_t>(c.w_cols) * (c.w_type == ELEM_BF16 ? 2 : 4)) % 16 == 0);
+    return e;
 }
 
-__device__ __forceinline__ void epi_update(const LaunchList& L, const EpiCtx& c, int r, int col, float v) {
-    const int64_t wi = c.transposed ? static_cast<int64_t>(col) * c.w_cols + r
-                                    : static_cast<int64_t>(r) * c.w_cols + col;
-    const float w = load_elem(c.w, wi, c.w_type);
-    store_elem(c.w, wi, c.w_type, fmaf(-c.lrs, v, L.decay * w));
+// Same formula, same operation order as epi_value (epilogue.cuh).
+__device__ __forceinline__ float epi_v(const EpiRegs& e, int r, int c, float acc, float aux) {
+    float t = e.c_acc * acc;
+    if (r == c) t += e.c_diag;
+    if (e.aux) t = fmaf(e.c_aux, aux, t);
+    return e.alpha * t;
 }
 
-// Element (r, col) with r < M, col < N.
-__device__ __forceinline__ void epi_element(const GemmGroup& g, const EpiCtx& c, const LaunchList& L,
-                                            int r, int col, float acc) {
-    if (g.mode == EPI_STORE && g.sym && r < col) return;
-    const float v = epi_value(g, c, r, col, acc, epi_aux(g, c, r, col));
-    if (g.mode == EPI_UPDATE) {
-        epi_update(L, c, r, col, v);
+// Element (r, col), r < M, col < N, with the parameters in registers: the
+// per-element path of the fp32 FFMA kernel (same formula as the chunked
+// tensor-core epilogue).
+__device__ __forceinline__ void epi_element_regs(const EpiRegs& e, int r, int col, float acc) {
+    if (e.mode == EPI_STORE && e.sym && r < col) return;
+    float aux = 0.0f;
+    if (e.aux) {
+        const int64_t i = e.aux_sym ? static_cast<int64_t>(col) * e.aux_ld + r : static_cast<int64_t>(r) * e.aux_ld + col;
+        aux = load_elem(e.aux, i, e.aux_type);
+    }
+    const float v = epi_v(e, r, col, acc, aux);
+    if (e.mode == EPI_UPDATE) {
+        const int64_t wi = e.transposed ? static_cast<int64_t>(col) * e.w_cols + r
+                                        : static_cast<int64_t>(r) * e.w_cols + col;
+        const float w = load_elem(e.w, wi, e.w_type);
+        store_elem(e.w, wi, e.w_type, fmaf(-e.lrs, v, e.decay * w));
         return;
     }
-    epi_write(g, c, r, col, v);
-    if (g.sym && r > col) epi_write(g, c, col, r, v);
+#pragma unroll
+    for (int o = 0; o < 3; ++o) {
+        if (!e.out[o]) continue;
+        store_elem(e.out[o], static_cast<int64_t>(r) * e.out_ld[o] + col, e.out_type[o], v);
+        if (e.sym && r > col) store_elem(e.out[o], static_cast<int64_t>(col) * e.out_ld[o] + r, e.out_type[o], v);
+    }
 }
 
 }  // namespace dmuon

@@ -328,58 +328,6 @@ __device__ __forceinline__ TileCoord decode_tile(const LaunchList& L, int t) {
     return c;
 }
 
-// Epilogue parameters of one tile, held in registers (the group table lives in
-// global memory, and stores through generic pointers would otherwise force
-// the compiler to reload every field after each store).
-struct EpiRegs {
-    const char* aux;
-    char* out[3];
-    char* w;
-    float alpha, c_acc, c_diag, c_aux, lrs, decay;
-    int32_t M, N, mode, sym, aux_type, aux_sym, aux_ld, w_type, w_cols, transposed, w_vec;
-    int32_t out_ld[3], out_type[3];
-};
-
-__device__ __forceinline__ EpiRegs load_epi(const GemmGroup& g, const LaunchList& L, int mat) {
-    const EpiCtx c = make_epi_ctx(g, L, mat);
-    EpiRegs e;
-    e.aux = static_cast<const char*>(c.aux);
-#pragma unroll
-    for (int o = 0; o < 3; ++o) {
-        e.out[o] = static_cast<char*>(c.out[o]);
-        e.out_ld[o] = g.out_ld[o];
-        e.out_type[o] = g.out_type[o];
-    }
-    e.w = static_cast<char*>(c.w);
-    e.alpha = c.alpha;
-    e.c_acc = g.c_acc;
-    e.c_diag = g.c_diag;
-    e.c_aux = g.c_aux;
-    e.lrs = c.lrs;
-    e.decay = L.decay;
-    e.M = g.M;
-    e.N = g.N;
-    e.mode = g.mode;
-    e.sym = g.sym;
-    e.aux_type = g.aux_type;
-    e.aux_sym = g.aux_sym;
-    e.aux_ld = g.aux_ld;
-    e.w_type = c.w_type;
-    e.w_cols = c.w_cols;
-    e.transposed = c.transposed;
-    // 16-byte row access to W needs every row start on 16 bytes
-    e.w_vec = c.w && ((static_cast<int64_t>(c.w_cols) * (c.w_type == ELEM_BF16 ? 2 : 4)) % 16 == 0);
-    return e;
-}
-
-// Same formula, same operation order as epi_value (epilogue.cuh).
-__device__ __forceinline__ float epi_v(const EpiRegs& e, int r, int c, float acc, float aux) {
-    float t = e.c_acc * acc;
-    if (r == c) t += e.c_diag;
-    if (e.aux) t = fmaf(e.c_aux, aux, t);
-    return e.alpha * t;
-}
-
 // 8 consecutive elements at p[i .. i+7] (16- or 32-byte aligned).
 __device__ __forceinline__ void ld8(const char* p, int64_t i, int32_t t, float* v) {
     if (t == ELEM_BF16) {
