@@ -212,12 +212,18 @@ const char* dmuon_status_string(int status);
 /* ---- inspection (tests) ------------------------------------------------ */
 
 #define DMUON_BUF_X 0  /* packed u (and direct-route iterate 0) */
-#define DMUON_BUF_RF 1 /* Gram route: fp32 R after the last update; direct: fp32 A */
+#define DMUON_BUF_RF 1 /* Gram route: fp32 R after the last update; direct: fp32 A.  With the
+                          tensor-core m x m engine only its lower triangle is written (it is read
+                          only as the next polynomial's aux term). */
+#define DMUON_BUF_R_OPERAND 2 /* the operand copy of the same R / A that the products read
+                                 (bf16 on tensor cores, the fp32 buffer otherwise): both
+                                 triangles, bitwise symmetric */
 
-/* Byte offset into the bound workspace, leading dimension (elements) and
- * batch stride (elements) of buffer `which` of piece (wave, piece). */
+/* Byte offset into the bound workspace, leading dimension (elements), batch
+ * stride (elements) and element dtype (DMUON_BF16 | DMUON_FP32; may be NULL)
+ * of buffer `which` of piece (wave, piece). */
 int dmuon_debug_buffer(dmuon_handle_t h, int64_t wave, int64_t piece, int32_t which,
-                       uint64_t* offset, int64_t* ld, int64_t* batch_stride);
+                       uint64_t* offset, int64_t* ld, int64_t* batch_stride, int32_t* elem_type);
 
 /* ---- one small matrix without device allocation ------------------------
  *

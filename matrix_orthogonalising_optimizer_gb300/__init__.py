@@ -163,7 +163,8 @@ class Muon:
         return {k: (ms[i], cnt[i]) for i, k in enumerate(TIMER_NAMES)}
 
     def debug_buffer(self, wave, piece, which):
-        off, ld, bs = ctypes.c_uint64(), ctypes.c_int64(), ctypes.c_int64()
+        """(byte offset, leading dimension, batch stride, dtype 'bf16'|'fp32') of a workspace buffer."""
+        off, ld, bs, et = ctypes.c_uint64(), ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int32()
         _lib.check(self.lib.dmuon_debug_buffer(self.handle, wave, piece, which, ctypes.byref(off), ctypes.byref(ld),
-                                               ctypes.byref(bs)), "dmuon_debug_buffer")
-        return off.value, ld.value, bs.value
+                                               ctypes.byref(bs), ctypes.byref(et)), "dmuon_debug_buffer")
+        return off.value, ld.value, bs.value, "bf16" if et.value == BF16 else "fp32"

@@ -20,7 +20,7 @@ ERR_INVALID_ARG, ERR_ALIGN, ERR_NO_WORKSPACE, ERR_UNSUPPORTED_DTYPE = -1, -2, -3
 ERR_CUDA, ERR_DEVICE_TIMEOUT, ERR_UNSUPPORTED_DEVICE, ERR_WORKSPACE_TOO_SMALL = -5, -6, -7, -8
 MAX_NS_STEPS = 16
 TIMER_NAMES = ("momentum", "norm", "syrk", "ns", "final", "tc", "simt")
-BUF_X, BUF_RF = 0, 1
+BUF_X, BUF_RF, BUF_R_OPERAND = 0, 1, 2
 
 
 class Shape(ctypes.Structure):
@@ -61,7 +61,7 @@ SIGNATURES = {
     "dmuon_last_error": (c_char_p, []),
     "dmuon_status_string": (c_char_p, [c_int]),
     "dmuon_debug_buffer": (c_int, [c_void_p, c_int64, c_int64, c_int32, POINTER(c_uint64), POINTER(c_int64),
-                                   POINTER(c_int64)]),
+                                   POINTER(c_int64), POINTER(c_int32)]),
     "dmuon_step_noalloc": (c_int, [c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_int32, c_float, c_float,
                                    c_float, c_int32, c_void_p]),
 }

@@ -133,6 +133,7 @@ struct GroupSpec {
     Operand aux;
     bool aux_sym = false;
     Operand out[3];
+    bool out_lower_only[3] = {false, false, false};  // symmetric D: skip the mirror of this output
     int64_t slot_base = 0;
 };
 
@@ -168,6 +169,7 @@ int build_group(const GroupSpec& s, GemmGroup* g) {
         g->out_type[o] = s.out[o].type;
         g->out_ld[o] = static_cast<int32_t>(s.out[o].ld);
         g->out_bs[o] = s.out[o].bs;
+        g->out_mirror[o] = s.sym && !s.out_lower_only[o] ? 1 : 0;
     }
     if (s.kernel == kKernelTc) {
         // pair tiles: 256 rows (two CTAs of 128) x 256 columns
@@ -725,7 +727,10 @@ int dmuon_bind_workspace(dmuon_handle_t h, void* dev_ptr, size_t bytes) {
                     s.sym = true;
                     s.alpha = ALPHA_INV2;
                     s.out[0] = RF;
-                    if (eng == kKernelTc) s.out[1] = RB;
+                    if (eng == kKernelTc) {
+                        s.out[1] = RB;
+                        s.out_lower_only[0] = true;  // fp32 R: only the next P's aux, lower triangle
+                    }
                     if ((rc = add(G_SYRK, s))) return rc;
                 }
                 for (int first = 1; first >= 0; --first) {  // P = aI + bR + cR^2
@@ -734,7 +739,7 @@ int dmuon_bind_workspace(dmuon_handle_t h, void* dev_ptr, size_t bytes) {
                     s.c_diag = h->ns_a;
                     s.c_aux = h->ns_b;
                     s.aux = RF;
-                    s.aux_sym = true;
+                    s.aux_sym = eng != kKernelTc;  // lower triangle only: read R[r][c], r >= c
                     s.out[0] = P;
                     if (first) {
                         s.out[1] = Q0;
@@ -756,7 +761,10 @@ int dmuon_bind_workspace(dmuon_handle_t h, void* dev_ptr, size_t bytes) {
                 {  // R <- P (R P)
                     GroupSpec s = sym_spec(eng, P, RP);
                     s.out[0] = RF;
-                    if (eng == kKernelTc) s.out[1] = RB;
+                    if (eng == kKernelTc) {
+                        s.out[1] = RB;
+                        s.out_lower_only[0] = true;
+                    }
                     if ((rc = add(G_RUPD, s))) return rc;
                 }
                 for (int qb = 0; qb < 2; ++qb) {  // W update from inv * Q X
@@ -789,7 +797,10 @@ int dmuon_bind_workspace(dmuon_handle_t h, void* dev_ptr, size_t bytes) {
                     s.sym = true;
                     s.alpha = sk.alpha;
                     s.out[0] = AF;
-                    if (eng == kKernelTc) s.out[1] = AB;
+                    if (eng == kKernelTc) {
+                        s.out[1] = AB;
+                        s.out_lower_only[0] = true;  // fp32 A: only B's aux, lower triangle
+                    }
                     if ((rc = add(sk.kind, s))) return rc;
                 }
                 {  // B = bA + cA^2
@@ -797,7 +808,7 @@ int dmuon_bind_workspace(dmuon_handle_t h, void* dev_ptr, size_t bytes) {
                     s.c_acc = h->ns_c;
                     s.c_aux = h->ns_b;
                     s.aux = AF;
-                    s.aux_sym = true;
+                    s.aux_sym = eng != kKernelTc;
                     s.out[0] = BB;
                     if ((rc = add(D_A2, s))) return rc;
                 }
@@ -953,16 +964,18 @@ int dmuon_get_timing(dmuon_handle_t h, double* ms, int64_t* launches, int32_t n)
 }
 
 int dmuon_debug_buffer(dmuon_handle_t h, int64_t wave, int64_t piece, int32_t which, uint64_t* offset, int64_t* ld,
-                       int64_t* batch_stride) {
+                       int64_t* batch_stride, int32_t* elem_type) {
     if (!h || wave < 0 || wave >= static_cast<int64_t>(h->waves.size()) || piece < 0 ||
         piece >= static_cast<int64_t>(h->waves[wave].pieces.size()) || !offset || !ld || !batch_stride)
         return fail(DMUON_ERR_INVALID_ARG, "bad buffer query");
     const Piece& p = h->waves[wave].pieces[piece];
     const Bucket& b = h->buckets[p.bucket];
-    const int k = which == DMUON_BUF_X ? BUF_X0 : (which == DMUON_BUF_RF ? BUF_RF : -1);
+    int k = which == DMUON_BUF_X ? BUF_X0 : (which == DMUON_BUF_RF ? BUF_RF : -1);
+    if (which == DMUON_BUF_R_OPERAND) k = b.buf_bytes[BUF_RB] ? BUF_RB : (b.buf_bytes[BUF_AB] ? BUF_AB : BUF_RF);
     if (k < 0 || !b.buf_bytes[k]) return fail(DMUON_ERR_INVALID_ARG, "unknown buffer");
     *offset = h->off_waves + p.off[k];
     *ld = static_cast<int64_t>(up(static_cast<uint64_t>(k == BUF_X0 ? b.n : b.m), 8));
+    if (elem_type) *elem_type = b.buf_type[k] == ELEM_BF16 ? DMUON_BF16 : DMUON_FP32;
     *batch_stride = b.buf_bytes[k] / esz(b.buf_type[k]);
     return DMUON_OK;
 }

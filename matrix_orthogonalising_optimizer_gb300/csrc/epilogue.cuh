@@ -6,7 +6,8 @@
 // aux = R), the Gram product R0 = inv^2 X X^T, the direct-route iterate
 // X' = alpha (a X + B X), and the plain products.  It then either stores v
 // (fp32 and/or the operand dtype; symmetric results store the lower triangle
-// and its mirror, so they are bitwise symmetric), or applies the Muon update
+// and, for outputs read as operands, its mirror, so they are bitwise
+// symmetric), or applies the Muon update
 //   W = (1 - lr*wd) W - lr*s*v
 // in W's own orientation (transposed back for tall matrices).
 #pragma once
@@ -75,7 +76,7 @@ struct EpiRegs {
     char* w;
     float alpha, c_acc, c_diag, c_aux, lrs, decay;
     int32_t M, N, mode, sym, aux_type, aux_sym, aux_ld, w_type, w_cols, transposed, w_vec;
-    int32_t out_ld[3], out_type[3];
+    int32_t out_ld[3], out_type[3], out_mirror[3];
 };
 
 __device__ __forceinline__ EpiRegs load_epi(const GemmGroup& g, const LaunchList& L, int mat) {
@@ -87,6 +88,7 @@ __device__ __forceinline__ EpiRegs load_epi(const GemmGroup& g, const LaunchList
         e.out[o] = static_cast<char*>(c.out[o]);
         e.out_ld[o] = g.out_ld[o];
         e.out_type[o] = g.out_type[o];
+        e.out_mirror[o] = g.sym && g.out_mirror[o];
     }
     e.w = static_cast<char*>(c.w);
     e.alpha = c.alpha;
@@ -140,7 +142,8 @@ __device__ __forceinline__ void epi_element_regs(const EpiRegs& e, int r, int co
     for (int o = 0; o < 3; ++o) {
         if (!e.out[o]) continue;
         store_elem(e.out[o], static_cast<int64_t>(r) * e.out_ld[o] + col, e.out_type[o], v);
-        if (e.sym && r > col) store_elem(e.out[o], static_cast<int64_t>(col) * e.out_ld[o] + r, e.out_type[o], v);
+        if (e.out_mirror[o] && r > col)
+            store_elem(e.out[o], static_cast<int64_t>(col) * e.out_ld[o] + r, e.out_type[o], v);
     }
 }
 

@@ -481,7 +481,7 @@ __device__ __forceinline__ void epi_finish(const EpiRegs& e, int r, int c0, floa
                 for (int j = 0; j < CH; ++j)
                     if (j < ncol && (!e.sym || r >= c0 + j)) store_elem(e.out[o], rb + c0 + j, e.out_type[o], v[j]);
             }
-            if (e.sym) {
+            if (e.out_mirror[o]) {
 #pragma unroll
                 for (int j = 0; j < CH; ++j)
                     if (j < ncol && r > c0 + j)

@@ -91,6 +91,7 @@ struct GemmGroup {
     int64_t out_bs[3];
     int32_t out_ld[3];
     int32_t out_type[3];
+    int32_t out_mirror[3];  // symmetric D: also store the upper triangle of this output
 };
 
 // Passed by value to every GEMM launch.

@@ -159,23 +159,36 @@ def test_deterministic_and_batching_invariant():
         assert torch.equal(alone[0], a[i])
 
 
-def test_gram_buffer_bitwise_symmetric():
-    # the last Gram-route R and the last direct-route A = X X^T are stored as
-    # lower triangle plus mirror, so they are bitwise symmetric
-    shapes = [(320, 704)] * 2 + [(300, 960)] + [(520, 1100)]
+def test_symmetric_operands_bitwise():
+    # The R / A that the products read (bf16 on tensor cores, fp32 for the
+    # FFMA engine) is stored as lower triangle plus mirror: bitwise symmetric.
+    # The fp32 copy kept for the next polynomial's aux term holds the same
+    # lower triangle before rounding.
+    shapes = [(320, 704)] * 2 + [(300, 960)] + [(520, 1100)] + [(100, 400)] * 2
     inputs = make_inputs(shapes, "bf16", 20)
     _, _, muon = run_step(shapes, inputs, "bf16", lr=LR, beta=BETA, wd=WD)
     ws = muon.workspace
     buckets = muon.buckets()
-    assert {b["route"] for b in buckets} == {1, 2}
+    assert {b["route"] for b in buckets} == {1, 2} and {b["engine"] for b in buckets} == {0, 1}
+
+    def matrices(p, which, m, nb):
+        off, ld, bs, dt = muon.debug_buffer(0, p, which)
+        tdt, esz = (torch.bfloat16, 2) if dt == "bf16" else (torch.float32, 4)
+        raw = ws[off: off + nb * bs * esz].view(tdt).cpu().view(nb, bs)
+        return [raw[j, : m * ld].view(m, ld)[:, :m] for j in range(nb)], dt
+
     for p, (bi, start, nb) in enumerate(muon.waves()[0]):
         m = buckets[bi]["m"]
-        off, ld, bs = muon.debug_buffer(0, p, 1)
-        raw = ws[off: off + nb * bs * 4].view(torch.float32).cpu().view(nb, bs)
-        for j in range(nb):
-            r = raw[j, : m * ld].view(m, ld)[:, :m]
-            assert torch.equal(r, r.t())
-            assert torch.isfinite(r).all()
+        ops, dt = matrices(p, 2, m, nb)
+        fps, _ = matrices(p, 1, m, nb)
+        low = torch.tril(torch.ones(m, m, dtype=torch.bool))
+        for op, fp in zip(ops, fps):
+            assert torch.equal(op, op.t())
+            assert torch.isfinite(op.float()).all()
+            if dt == "bf16":
+                assert torch.equal(fp.to(torch.bfloat16)[low], op[low])
+            else:
+                assert torch.equal(fp, op)
 
 
 def test_workspace_budget_waves():
