@@ -328,36 +328,119 @@ __device__ __forceinline__ TileCoord decode_tile(const LaunchList& L, int t) {
     return c;
 }
 
-// 8 consecutive elements at p[i .. i+7] (16- or 32-byte aligned).
-__device__ __forceinline__ void ld8(const char* p, int64_t i, int32_t t, float* v) {
-    if (t == ELEM_BF16) {
-        const uint4 q = *reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p) + i);
-        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&q);
+// Warp-cooperative row segments.  After tcgen05.ld lane i of a warp holds row
+// r0 + i, columns c0 .. c0+15: a 16-byte access per lane would then touch 32
+// different rows (32 L2 requests, each for half a 32-byte sector of fp32 or
+// bf16 data).  Regrouping the data between lanes first makes each access
+// instruction cover whole row segments: bf16 rows (32 bytes) are swapped in
+// halves between lanes i and i^1, so one instruction writes 16 full sectors;
+// fp32 rows (64 bytes) are transposed as 4 x 4 blocks of 16 bytes inside each
+// lane quad, so one instruction writes 8 rows x 64 contiguous bytes.  Loads
+// use the same layouts in reverse.  All 32 lanes must call these; rows >= M
+// are neither read (zero) nor written.
+constexpr unsigned kFullMask = 0xffffffffu;
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__device__ __forceinline__ float2 unpack_bf16x2(uint32_t u) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u));
+}
+
+// 4 x 4 transpose of 16-byte blocks within each lane quad: block q of lane
+// i (words 4q .. 4q+3) ends in block i of lane q.  Its own inverse.
+template <typename T>
+__device__ __forceinline__ void quad_transpose(T (&w)[16], int lane) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const float2 f = __bfloat1622float2(h[k]);
-            v[2 * k] = f.x;
-            v[2 * k + 1] = f.y;
+    for (int s = 2; s >= 1; s >>= 1) {
+        const bool hi = (lane & s) != 0;
+#pragma unroll
+        for (int q0 = 0; q0 < 4; ++q0) {
+            if (q0 & s) continue;
+            const int q1 = q0 | s;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const T send = hi ? w[4 * q0 + k] : w[4 * q1 + k];
+                const T recv = __shfl_xor_sync(kFullMask, send, s);
+                w[4 * q0 + k] = hi ? recv : w[4 * q0 + k];
+                w[4 * q1 + k] = hi ? w[4 * q1 + k] : recv;
+            }
         }
-    } else {
-        const float4* q = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(p) + i);
-        const float4 a = q[0], b = q[1];
-        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
     }
 }
 
-__device__ __forceinline__ void st8(char* p, int64_t i, int32_t t, const float* v) {
-    if (t == ELEM_BF16) {
-        uint4 q;
-        __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&q);
+// fp32 rows are transposed in v itself (no copy: the registers are scarce);
+// `restore` transposes v back for later uses.
+__device__ __forceinline__ void st_rows(char* base, int32_t type, int64_t ld, int r0, int c0, int lane,
+                                        float (&v)[CH], int M, bool restore) {
+    if (type == ELEM_BF16) {
+        uint32_t w[8];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) h[k] = __floats2bfloat162_rn(v[2 * k], v[2 * k + 1]);
-        *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p) + i) = q;
+        for (int k = 0; k < 8; ++k) w[k] = pack_bf16x2(v[2 * k], v[2 * k + 1]);
+        const bool odd = lane & 1;
+        uint32_t d0[4], d1[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t keep = odd ? w[4 + k] : w[k];
+            const uint32_t recv = __shfl_xor_sync(kFullMask, odd ? w[k] : w[4 + k], 1);
+            d0[k] = odd ? recv : keep;  // row (lane & ~1), half `odd`
+            d1[k] = odd ? keep : recv;  // row (lane | 1),  half `odd`
+        }
+        const int ra = r0 + (lane & ~1);
+        __nv_bfloat16* p = reinterpret_cast<__nv_bfloat16*>(base) + static_cast<int64_t>(ra) * ld + c0 + 8 * odd;
+        if (ra < M) *reinterpret_cast<uint4*>(p) = make_uint4(d0[0], d0[1], d0[2], d0[3]);
+        if (ra + 1 < M) *reinterpret_cast<uint4*>(p + ld) = make_uint4(d1[0], d1[1], d1[2], d1[3]);
     } else {
-        float4* q = reinterpret_cast<float4*>(reinterpret_cast<float*>(p) + i);
-        q[0] = make_float4(v[0], v[1], v[2], v[3]);
-        q[1] = make_float4(v[4], v[5], v[6], v[7]);
+        quad_transpose(v, lane);
+        const int rq = r0 + (lane & ~3);
+        float* p = reinterpret_cast<float*>(base) + static_cast<int64_t>(rq) * ld + c0 + 4 * (lane & 3);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (rq + j < M)
+                *reinterpret_cast<float4*>(p + j * ld) = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        if (restore) quad_transpose(v, lane);
+    }
+}
+
+__device__ __forceinline__ void ld_rows(const char* base, int32_t type, int64_t ld, int r0, int c0, int lane,
+                                        float (&x)[CH], int M) {
+    if (type == ELEM_BF16) {
+        const bool odd = lane & 1;
+        const int ra = r0 + (lane & ~1);
+        const __nv_bfloat16* p =
+            reinterpret_cast<const __nv_bfloat16*>(base) + static_cast<int64_t>(ra) * ld + c0 + 8 * odd;
+        uint4 a = make_uint4(0, 0, 0, 0), b = make_uint4(0, 0, 0, 0);
+        if (ra < M) a = *reinterpret_cast<const uint4*>(p);
+        if (ra + 1 < M) b = *reinterpret_cast<const uint4*>(p + ld);
+        const uint32_t d0[4] = {a.x, a.y, a.z, a.w}, d1[4] = {b.x, b.y, b.z, b.w};
+        uint32_t w[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t recv = __shfl_xor_sync(kFullMask, odd ? d0[k] : d1[k], 1);
+            w[k] = odd ? recv : d0[k];
+            w[4 + k] = odd ? d1[k] : recv;
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float2 f = unpack_bf16x2(w[k]);
+            x[2 * k] = f.x;
+            x[2 * k + 1] = f.y;
+        }
+    } else {
+        const int rq = r0 + (lane & ~3);
+        const float* p = reinterpret_cast<const float*>(base) + static_cast<int64_t>(rq) * ld + c0 + 4 * (lane & 3);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            float4 q = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            if (rq + j < M) q = *reinterpret_cast<const float4*>(p + j * ld);
+            x[4 * j] = q.x;
+            x[4 * j + 1] = q.y;
+            x[4 * j + 2] = q.z;
+            x[4 * j + 3] = q.w;
+        }
+        quad_transpose(x, lane);
     }
 }
 
@@ -373,15 +456,12 @@ __device__ __forceinline__ void st8(char* p, int64_t i, int32_t t, const float* 
 
 // CH elements of row r from columns c0.. of a row-major matrix (or of its
 // transpose when by_col: element (r, c) read at [c][r]).
-__device__ __forceinline__ void load_row(const char* base, int32_t type, int32_t ld, bool by_col, bool vec,
-                                         int r, int c0, int ncol, float (&x)[CH]) {
+__device__ __forceinline__ void load_row(const char* base, int32_t type, int32_t ld, bool by_col, int r, int c0,
+                                         int ncol, float (&x)[CH]) {
     if (by_col) {
 #pragma unroll
         for (int j = 0; j < CH; ++j)
             x[j] = j < ncol ? load_elem(base, static_cast<int64_t>(c0 + j) * ld + r, type) : 0.0f;
-    } else if (vec) {
-#pragma unroll
-        for (int j = 0; j < CH; j += 8) ld8(base, static_cast<int64_t>(r) * ld + c0 + j, type, x + j);
     } else {
 #pragma unroll
         for (int j = 0; j < CH; ++j)
@@ -422,8 +502,8 @@ __device__ __forceinline__ void epi_prefetch(const EpiRegs& e, int r, int r0, in
 }
 
 // Prefetched input of a chunk: W for the update, else the aux operand.
-__device__ __forceinline__ void epi_load(const EpiRegs& e, int r, int c0, float (&x)[CH]) {
-    if (r >= e.M || c0 >= e.N) return;
+__device__ __forceinline__ void epi_load(const EpiRegs& e, int r, int r0, int lane, int c0, float (&x)[CH]) {
+    if (r0 >= e.M || c0 >= e.N) return;  // warp-uniform
     const int ncol = min(CH, e.N - c0);
     const bool full = ncol == CH;
     const char* base;
@@ -445,13 +525,16 @@ __device__ __forceinline__ void epi_load(const EpiRegs& e, int r, int c0, float 
     } else {
         return;
     }
-    load_row(base, type, ld, by_col, vec, r, c0, ncol, x);
+    if (vec && !by_col) ld_rows(base, type, ld, r0, c0, lane, x, e.M);
+    else if (r < e.M) load_row(base, type, ld, by_col, r, c0, ncol, x);
 }
 
 // v (computed in place of the accumulator values) and, for the update, the new
 // W (in place of the loaded W values), to keep the register footprint low.
-__device__ __forceinline__ void epi_finish(const EpiRegs& e, int r, int c0, float (&v)[CH], float (&x)[CH]) {
-    if (r >= e.M) return;
+__device__ __forceinline__ void epi_finish(const EpiRegs& e, int r, int r0, int lane, int c0, float (&v)[CH],
+                                           float (&x)[CH]) {
+    if (r0 >= e.M) return;  // warp-uniform: no row of this warp exists
+    const bool valid = r < e.M;
     const int ncol = min(CH, e.N - c0);
     const bool full = ncol == CH;
     const bool upd = e.mode == EPI_UPDATE;
@@ -459,7 +542,10 @@ __device__ __forceinline__ void epi_finish(const EpiRegs& e, int r, int c0, floa
         // the update that also has an aux term (direct route: a X + B X) reads
         // the aux chunk here; x already holds W
         float a[CH];
-        load_row(e.aux, e.aux_type, e.aux_ld, e.aux_sym, full, r, c0, ncol, a);
+#pragma unroll
+        for (int j = 0; j < CH; ++j) a[j] = 0.0f;
+        if (full && !e.aux_sym) ld_rows(e.aux, e.aux_type, e.aux_ld, r0, c0, lane, a, e.M);
+        else if (valid) load_row(e.aux, e.aux_type, e.aux_ld, e.aux_sym, r, c0, ncol, a);
 #pragma unroll
         for (int j = 0; j < CH; ++j) v[j] = epi_v(e, r, c0 + j, v[j], a[j]);
     } else {
@@ -468,43 +554,44 @@ __device__ __forceinline__ void epi_finish(const EpiRegs& e, int r, int c0, floa
     }
 
     if (!upd) {
-        const bool below = !e.sym || c0 + CH - 1 < r;  // every column of the chunk is stored directly
+        // every column of the chunk is stored directly in all 32 rows of the warp
+        const bool coop = full && (!e.sym || c0 + CH - 1 < r0);
+        // last output first, and each output's mirror before its rows: an fp32
+        // row store leaves v transposed unless something still needs it
 #pragma unroll
-        for (int o = 0; o < 3; ++o) {
+        for (int o = 2; o >= 0; --o) {
             if (!e.out[o]) continue;
-            const int64_t rb = static_cast<int64_t>(r) * e.out_ld[o];
-            if (full && below) {
-#pragma unroll
-                for (int j = 0; j < CH; j += 8) st8(e.out[o], rb + c0 + j, e.out_type[o], v + j);
-            } else {
-#pragma unroll
-                for (int j = 0; j < CH; ++j)
-                    if (j < ncol && (!e.sym || r >= c0 + j)) store_elem(e.out[o], rb + c0 + j, e.out_type[o], v[j]);
-            }
-            if (e.out_mirror[o]) {
+            if (valid && e.out_mirror[o]) {
 #pragma unroll
                 for (int j = 0; j < CH; ++j)
                     if (j < ncol && r > c0 + j)
                         store_elem(e.out[o], static_cast<int64_t>(c0 + j) * e.out_ld[o] + r, e.out_type[o], v[j]);
             }
+            if (coop) {
+                st_rows(e.out[o], e.out_type[o], e.out_ld[o], r0, c0, lane, v, e.M, o > 0);
+            } else if (valid) {
+                const int64_t rb = static_cast<int64_t>(r) * e.out_ld[o];
+#pragma unroll
+                for (int j = 0; j < CH; ++j)
+                    if (j < ncol && (!e.sym || r >= c0 + j)) store_elem(e.out[o], rb + c0 + j, e.out_type[o], v[j]);
+            }
         }
         return;
     }
     // Muon update W = decay*W - lr*s*v in W's own orientation (x holds W)
-    float* w = x;
+    float (&w)[CH] = x;
 #pragma unroll
     for (int j = 0; j < CH; ++j) w[j] = fmaf(-e.lrs, v[j], e.decay * x[j]);
     if (!e.transposed) {
         const int64_t rb = static_cast<int64_t>(r) * e.w_cols;
         if (full && e.w_vec) {
-#pragma unroll
-            for (int j = 0; j < CH; j += 8) st8(e.w, rb + c0 + j, e.w_type, w + j);
-        } else {
+            st_rows(e.w, e.w_type, e.w_cols, r0, c0, lane, w, e.M, false);
+        } else if (valid) {
 #pragma unroll
             for (int j = 0; j < CH; ++j)
                 if (j < ncol) store_elem(e.w, rb + c0 + j, e.w_type, w[j]);
         }
-    } else {
+    } else if (valid) {
 #pragma unroll
         for (int j = 0; j < CH; ++j)
             if (j < ncol) store_elem(e.w, static_cast<int64_t>(c0 + j) * e.w_cols + r, e.w_type, w[j]);
@@ -766,7 +853,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
             const uint32_t use = static_cast<uint32_t>(it >> 1);
             const EpiRegs e = load_epi(g, L, tc.mat);
             const int tm = 2 * tc.tm + rank;  // this CTA's 128-row tile
-            const int r = tm * BM + q * 32 + lane;
+            const int r0w = tm * BM + q * 32;  // first row of this warp
+            const int r = r0w + lane;
             const int row_last = tm * BM + BM - 1;
             // chunks of this warp that hold stored columns
             constexpr int kChunks = (BN / 2) / CH;
@@ -809,7 +897,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
                 }
             } else {
             float xin[CH];
-            if (nch > 0) epi_load(e, r, tc.tn * BN + ch0 * CH, xin);
+            if (nch > 0) epi_load(e, r, r0w, lane, tc.tn * BN + ch0 * CH, xin);
             if (!mbar_wait(&S.acc_full[buf], use & 1, L.status)) break;
             tc_fence_after();
             for (int kc = 0; kc < nch; ++kc) {
@@ -817,11 +905,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
                 float x[CH];
 #pragma unroll
                 for (int j = 0; j < CH; ++j) x[j] = xin[j];
-                if (kc + 1 < nch) epi_load(e, r, c0 + CH, xin);
+                if (kc + 1 < nch) epi_load(e, r, r0w, lane, c0 + CH, xin);
                 float v[CH];
                 __syncwarp();
                 tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN + (ch0 + kc) * CH), v);
-                epi_finish(e, r, c0, v, x);
+                epi_finish(e, r, r0w, lane, c0, v, x);
             }
             }
             __syncwarp();
