@@ -10,26 +10,35 @@
 // (section 2.2 "batching").
 //
 // Layout: clusters of two CTAs (one CTA per SM), persistent over a dynamic
-// schedule of 256 x 256 pair tiles taken in order from a per-launch counter.  Each CTA of a pair computes
-// 128 rows; the pair shares the 256-column B tile, each CTA loading one half
-// with a TMA multicast into both, which cuts L2 reads per FLOP by a third.
-// Per CTA:
-//   warp 0      one thread issues TMA loads into a 4-stage shared-memory ring
-//               (a stage is free once both CTAs' MMAs have read it)
-//   warp 1      allocates 512 TMEM columns; one thread issues tcgen05.mma
-//               (kind::f16, bf16 operands, fp32 accumulation) into one of two
-//               128 x 256 fp32 accumulators
-//   warps 2..9  epilogue, two per TMEM lane quarter (128 columns each):
-//               tcgen05.ld the accumulator (row per thread), apply
-//               the fused epilogue, store; releases the accumulator so the
-//               next tile's MMAs overlap this tile's epilogue.
+// schedule of 256 x 256 pair tiles taken in order from a per-launch counter.
+// The pair runs one tcgen05.mma.cta_group::2 of M = 256, N = 256: CTA rank r
+// holds rows 128 r .. 128 r + 127 of the A tile and columns 128 r ..
+// 128 r + 127 of the B tile in its own shared memory, and receives rows
+// 128 r .. of the 256 x 256 fp32 accumulator in its own TMEM.  A CTA thus
+// stores 32 KB per 64-deep K slab (a lone 128 x 256 tile needs 48 KB), so the
+// ring holds six stages.
+//   warp 0      (both CTAs) one thread issues the CTA's TMA loads into a
+//               6-stage ring; the bytes of both CTAs complete on the
+//               leader's (rank 0) full barrier
+//   warp 1      (both CTAs) allocates 512 TMEM columns as a pair; in the
+//               leader one thread issues the MMAs (kind::f16, bf16 operands,
+//               fp32 accumulation) into one of two 256-column accumulators
+//               and commits to both CTAs' barriers
+//   warps 2..9  (both CTAs) epilogue, two per TMEM lane quarter (128 columns
+//               each): tcgen05.ld the accumulator (row per thread), apply the
+//               fused epilogue, store; then release the accumulator to the
+//               leader so the next tile's MMAs overlap this tile's epilogue.
 // Operands use the 128-byte swizzle.  A is K-major (row-major M x K).  B is
 // K-major (stored N x K: symmetric operands and the Gram product) or MN-major
 // (stored K x N: the m x n iterate multiplied from the left).
 //
 // Every mbarrier wait is bounded (about 2 s of %globaltimer); on expiry the
 // waiting thread records DEV_TIMEOUT in the status word and leaves its loop,
-// so a broken pipeline ends the kernel instead of hanging the GPU.
+// so a broken pipeline ends the kernel instead of hanging the GPU.  The
+// per-stage ring waits (full, empty) only order the async proxy's copies and
+// MMAs, which their mbarrier transactions already cover, and use CTA scope; a
+// cluster-scope acquire on them cost about 10 % of the step.  The tile ring
+// and the accumulator hand-off between the CTAs' threads use cluster scope.
 #include <cuda_bf16.h>
 
 #include "epilogue.cuh"
@@ -42,28 +51,29 @@ constexpr int BN = kTcBN;
 constexpr int STAGES = kTcStages;
 constexpr int SLAB_K = kTcSlabBytes / 2;        // 64 bf16 per 128-byte row
 constexpr int UMMA_K = 16;                      // bf16 K per tcgen05.mma
-constexpr int A_BYTES = BM * kTcSlabBytes;      // 16 KB
-constexpr int B_BYTES = BN * kTcSlabBytes;      // 32 KB
+constexpr int kPair = kTcPair;                  // CTAs per cluster sharing one MMA
+constexpr int A_BYTES = BM * kTcSlabBytes;      // 16 KB: this CTA's 128 rows of A
+constexpr int B_BYTES = (BN / kPair) * kTcSlabBytes;  // 16 KB: this CTA's 128 columns of B
 constexpr int MN_BOX_BYTES = SLAB_K * 128;      // one MN-major box: 64 K-rows x 128 B
-constexpr uint32_t STAGE_TX = A_BYTES + B_BYTES;
+constexpr uint32_t STAGE_TX = kPair * (A_BYTES + B_BYTES);  // both CTAs' bytes, on the leader's barrier
 constexpr uint32_t TMEM_COLS = 512;             // two 256-column accumulators
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr int kTileRing = 4;
 constexpr int kTStageLd = 132;  // 128 W columns + 4 pad; 528-byte rows keep float4 reads aligned
-// readers of a tile slot: per CTA the MMA thread and the 8 epilogue warps,
-// plus the partner's producer
-constexpr uint32_t kTileReaders = 2 * (1 + (kTcThreads - 64) / 32) + 1;
+constexpr int kEpiWarps = (kTcThreads - 64) / 32;
+// readers of a tile slot: the 8 epilogue warps of each CTA, the leader's MMA
+// thread and the partner's producer
+constexpr uint32_t kTileReaders = kPair * kEpiWarps + 2;
 constexpr int CH = 16;                          // epilogue chunk: columns per tcgen05.ld
-constexpr int kPair = kTcPair;                   // CTAs per cluster sharing the B tile
 constexpr uint16_t kPairMask = (1u << kPair) - 1;
 
 struct __align__(1024) Smem {
     uint8_t a[STAGES][A_BYTES];
     uint8_t b[STAGES][B_BYTES];
-    uint64_t full[STAGES];
-    uint64_t empty[STAGES];
-    uint64_t acc_full[2];
-    uint64_t acc_empty[2];
+    uint64_t full[STAGES];       // leader only: both CTAs' loads of a stage landed
+    uint64_t empty[STAGES];      // the pair's MMAs have read the stage (count 1)
+    uint64_t acc_full[2];        // the accumulator is complete (count 1)
+    uint64_t acc_empty[2];       // leader only: every epilogue warp of both CTAs is done
     uint64_t tile_full[kTileRing];   // a tile index is in tile_slot (count 1)
     uint64_t tile_empty[kTileRing];  // leader only: every reader of both CTAs is done
     int32_t tile_slot[kTileRing];
@@ -90,10 +100,6 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
 __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(saddr(bar)), "r"(bytes)
                  : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr(bar)) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
@@ -128,23 +134,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_
     return mbar_wait_slow(bar, parity, status);
 }
 
-__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1,
-                                            int c2) {
+// TMA box load into this CTA's shared memory whose completion is counted on
+// an mbarrier of either CTA of the pair (`bar` is a shared::cluster address).
+__device__ __forceinline__ void tma_load_3d_pair(void* dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,
+                                                 int c2) {
     asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(saddr(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(saddr(bar))
-        : "memory");
-}
-
-// Same, multicast: the box lands at the same shared-memory offset in every CTA
-// of the cluster named in `mask`, and each signals its own mbarrier there.
-__device__ __forceinline__ void tma_load_3d_mc(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1,
-                                               int c2, uint16_t mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(saddr(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(saddr(bar)), "h"(mask)
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
         : "memory");
 }
 
@@ -223,10 +220,11 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
     return d;
 }
 
-// Instruction descriptor: kind::f16, bf16 A/B, fp32 D, M = 128, N = 256.
+// Instruction descriptor: kind::f16, bf16 A/B, fp32 D, M = 256 (the pair),
+// N = 256.
 __host__ __device__ constexpr uint32_t make_idesc(bool b_mn_major) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
-           (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(BM >> 4) << 24);
+           (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>((kPair * BM) >> 4) << 24);
 }
 
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
@@ -234,21 +232,16 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t 
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
         : "memory");
-}
-
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(saddr(bar))
-                 : "memory");
 }
 
 // Arrive on the mbarrier at this offset in every CTA of `mask` once this
 // thread's MMAs so far have completed.
 __device__ __forceinline__ void umma_commit_mc(uint64_t* bar, uint16_t mask) {
     asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
             saddr(bar)),
         "h"(mask)
         : "memory");
@@ -686,12 +679,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&S.full[s], 1);
-            mbar_init(&S.empty[s], kPair);  // both CTAs' MMAs release a stage
+            mbar_init(&S.full[s], 1);   // the leader's expect_tx; the bytes of both CTAs
+            mbar_init(&S.empty[s], 1);  // the leader's MMA commit
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&S.acc_full[b], 1);
-            mbar_init(&S.acc_empty[b], kTcThreads - 64);
+            mbar_init(&S.acc_empty[b], kPair * kEpiWarps);
         }
         for (int i = 0; i < kTileRing; ++i) {
             mbar_init(&S.tile_full[i], 1);
@@ -700,14 +693,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(&S.tmem_base)),
+        // one warp of each CTA: the same columns in both CTAs' TMEM
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(&S.tmem_base)),
                      "r"(TMEM_COLS)
                      : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
     }
     tc_fence_before();
     __syncthreads();
-    cluster_sync();  // the partner's barriers exist before any multicast targets them
+    cluster_sync();  // the partner's barriers exist before any remote arrival targets them
     tc_fence_after();
     const uint32_t tmem = S.tmem_base;
     const int rank = static_cast<int>(cluster_rank());
@@ -749,27 +743,26 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
             const TileCoord tc = decode_tile(L, t);
             const GemmGroup* g = L.groups + L.idx[tc.gi];
             const int nkb = (g->K + SLAB_K - 1) / SLAB_K;
+            const int b_col = tc.tn * BN + rank * (BN / kPair);  // this CTA's 128 columns of B
             for (int kb = 0; kb < nkb; ++kb) {
                 if (!mbar_wait(&S.empty[stage], phase ^ 1, L.status)) {
                     ok = false;
                     break;
                 }
-                mbar_expect_tx(&S.full[stage], STAGE_TX);
+                if (rank == 0) mbar_expect_tx(&S.full[stage], STAGE_TX);
                 issued |= 1u << stage;
                 issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-                // own 128 rows of A; own half of the shared B tile, multicast to
-                // both CTAs of the pair (the partner sends the other half)
-                tma_load_3d(S.a[stage], &g->tma_a, &S.full[stage], kb * SLAB_K, (2 * tc.tm + rank) * BM, tc.mat);
+                // own 128 rows of A and own 128 columns of B, counted on the
+                // leader's barrier
+                const uint32_t fb = mapa(saddr(&S.full[stage]), 0);
+                tma_load_3d_pair(S.a[stage], &g->tma_a, fb, kb * SLAB_K, (2 * tc.tm + rank) * BM, tc.mat);
                 if (!g->b_mn_major) {
-                    tma_load_3d_mc(S.b[stage] + rank * (B_BYTES / kPair), &g->tma_b, &S.full[stage], kb * SLAB_K,
-                                   tc.tn * BN + rank * (BN / kPair), tc.mat, kPairMask);
+                    tma_load_3d_pair(S.b[stage], &g->tma_b, fb, kb * SLAB_K, b_col, tc.mat);
                 } else {
 #pragma unroll
-                    for (int i = 0; i < BN / 64 / kPair; ++i) {
-                        const int box = rank * (BN / 64 / kPair) + i;
-                        tma_load_3d_mc(S.b[stage] + box * MN_BOX_BYTES, &g->tma_b, &S.full[stage],
-                                       tc.tn * BN + 64 * box, kb * SLAB_K, tc.mat, kPairMask);
-                    }
+                    for (int i = 0; i < BN / 64 / kPair; ++i)
+                        tma_load_3d_pair(S.b[stage] + i * MN_BOX_BYTES, &g->tma_b, fb, b_col + 64 * i, kb * SLAB_K,
+                                         tc.mat);
                 }
                 if (++stage == STAGES) {
                     stage = 0;
@@ -778,23 +771,26 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
             }
         }
         if (!ok) {
-            // let copies already issued land before the CTA can exit
-            for (int s = 0; s < STAGES; ++s)
-                if (issued & (1u << s)) mbar_wait(&S.full[s], (issued_parity >> s) & 1u, L.status);
+            // let copies already issued land before the CTA can exit (the
+            // leader's barrier counts both CTAs' copies; the partner waits
+            // for the leader at the final cluster barrier)
+            if (rank == 0)
+                for (int s = 0; s < STAGES; ++s)
+                    if (issued & (1u << s)) mbar_wait(&S.full[s], (issued_parity >> s) & 1u, L.status);
         } else {
-            // wait for both MMAs' releases of the last ring round, so no
-            // arrival from the partner is still in flight towards this CTA
+            // wait for the MMA's releases of the last ring round, so no
+            // commit from the leader is still in flight towards this CTA
             // when the pair leaves through the final cluster barrier
             for (int i = 0; i < STAGES && ok; ++i) {
-                ok = mbar_wait(&S.empty[stage], phase ^ 1, L.status);
+                ok = mbar_wait_cluster(&S.empty[stage], phase ^ 1, L.status);
                 if (++stage == STAGES) {
                     stage = 0;
                     phase ^= 1;
                 }
             }
         }
-    } else if (warp == 1 && lane == 0) {
-        // ------------------------------------------------ MMA issuer
+    } else if (warp == 1 && lane == 0 && rank == 0) {
+        // ------------------------------------------------ MMA issuer (leader)
         uint32_t stage = 0, phase = 0;
         bool ok = true;
         int it = 0;
@@ -807,7 +803,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
             const int nkb = (g->K + SLAB_K - 1) / SLAB_K;
             const int buf = it & 1;
             const uint32_t use = static_cast<uint32_t>(it >> 1);
-            if (!mbar_wait(&S.acc_empty[buf], (use & 1) ^ 1, L.status)) break;
+            if (!mbar_wait_cluster(&S.acc_empty[buf], (use & 1) ^ 1, L.status)) break;
             tc_fence_after();
             const uint32_t d = tmem + static_cast<uint32_t>(buf * BN);
             const bool bmn = g->b_mn_major != 0;
@@ -835,7 +831,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
             }
             // also on failure: the commit tracks every MMA issued so far, so the
             // epilogue's wait on it covers them before TMEM is released
-            umma_commit(&S.acc_full[buf]);
+            umma_commit_mc(&S.acc_full[buf], kPairMask);
         }
     } else if (warp >= 2) {
         // ------------------------------------------------ epilogue
@@ -874,7 +870,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
                 float* stg = S.tstage[half];
                 float wn[4][4];
                 if (nch > 0) tw_load(e, tc.tn * BN + ch0 * CH, q, wc, wn);
-                const bool ready = mbar_wait(&S.acc_full[buf], use & 1, L.status);
+                const bool ready = mbar_wait_cluster(&S.acc_full[buf], use & 1, L.status);
                 if (!named_bar_and(1 + half, ready)) break;
                 tc_fence_after();
                 for (int kc = 0; kc < nch; ++kc) {
@@ -898,7 +894,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
             } else {
             float xin[CH];
             if (nch > 0) epi_load(e, r, r0w, lane, tc.tn * BN + ch0 * CH, xin);
-            if (!mbar_wait(&S.acc_full[buf], use & 1, L.status)) break;
+            if (!mbar_wait_cluster(&S.acc_full[buf], use & 1, L.status)) break;
             tc_fence_after();
             for (int kc = 0; kc < nch; ++kc) {
                 const int c0 = tc.tn * BN + (ch0 + kc) * CH;
@@ -912,21 +908,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
                 epi_finish(e, r, r0w, lane, c0, v, x);
             }
             }
-            __syncwarp();
             tc_fence_before();
-            mbar_arrive(&S.acc_empty[buf]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(mapa(saddr(&S.acc_empty[buf]), 0));
         }
     }
 
     tc_fence_before();
     __syncthreads();
-    // neither CTA leaves while the partner may still multicast into its shared
-    // memory or arrive on its barriers
+    // neither CTA leaves while the partner may still read its shared memory
+    // (the leader's MMAs) or arrive on its barriers
     cluster_sync();
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
     }
 }
 

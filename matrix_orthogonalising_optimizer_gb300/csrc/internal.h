@@ -14,9 +14,9 @@ namespace dmuon {
 constexpr int kTcBM = 128;
 constexpr int kTcBN = 256;
 constexpr int kTcSlabBytes = 128;  // one K slab row = one 128-byte swizzle row
-constexpr int kTcStages = 4;
+constexpr int kTcStages = 6;
 constexpr int kTcThreads = 320;    // warp 0 TMA, warp 1 MMA + TMEM, warps 2-9 epilogue
-constexpr int kTcPair = 2;         // CTAs per cluster sharing one B tile (multicast)
+constexpr int kTcPair = 2;         // CTAs per cluster running one cta_group::2 MMA
 
 // fp32 FFMA GEMM tile
 constexpr int kSimtBM = 64;
