@@ -225,6 +225,41 @@ const char* dmuon_status_string(int status);
 int dmuon_debug_buffer(dmuon_handle_t h, int64_t wave, int64_t piece, int32_t which,
                        uint64_t* offset, int64_t* ld, int64_t* batch_stride, int32_t* elem_type);
 
+/* ---- owner assignment (host only) --------------------------------------
+ *
+ * DMuon technical summary (gist.science), section 2.3 "compute-aware load
+ * balancing": every matrix gets one owner rank, which alone runs its update;
+ * the owners minimise the predicted makespan (largest per-rank sum of
+ * predicted costs), posed as a mixed-integer program, with a greedy fallback
+ * for very large instances.  The single-GPU step has no ranks: this computes
+ * the assignment for a multi-rank caller from costs it supplies (e.g. the
+ * plan's per-matrix FLOPs below, or measured per-bucket step times).
+ *
+ * costs:  host array of `count` finite costs >= 0 (any unit).
+ * ranks:  number of owner ranks, >= 1.
+ * method: DMUON_ASSIGN_GREEDY -- longest processing time first: matrices in
+ *         decreasing cost (ties: lower index first), each to the least-loaded
+ *         rank so far (ties: lower rank); any count.
+ *         DMUON_ASSIGN_EXACT -- the optimum of the makespan program (branch
+ *         and bound from the greedy solution); count <= 32, and an instance
+ *         whose search exceeds 2e8 nodes returns DMUON_ERR_INVALID_ARG.
+ * owner:  host array of `count` ranks in [0, ranks), written.
+ * makespan: if not NULL, the largest per-rank sum of the result, each rank's
+ *         costs added in increasing matrix index.
+ * Returns DMUON_OK or DMUON_ERR_INVALID_ARG (negative / non-finite cost, bad
+ * count, ranks or method, NULL array).  No device work. */
+#define DMUON_ASSIGN_GREEDY 0
+#define DMUON_ASSIGN_EXACT 1
+int dmuon_assign_owners(const double* costs, int64_t count, int32_t ranks, int32_t method, int32_t* owner,
+                        double* makespan);
+
+/* Per-matrix algorithmic FLOPs of one step at ns_steps, in the order of the
+ * plan's shapes (same formulas as dmuon_plan_flops, by each matrix's bucket
+ * route; their sum is dmuon_plan_flops' out[0]): a cost model for
+ * dmuon_assign_owners.  flops: host array of the plan's count.  Returns
+ * DMUON_OK or DMUON_ERR_INVALID_ARG. */
+int dmuon_plan_matrix_flops(dmuon_handle_t h, int32_t ns_steps, double* flops);
+
 /* ---- one small matrix without device allocation ------------------------
  *
  * No counterpart in the paper: an addition for callers that cannot allocate

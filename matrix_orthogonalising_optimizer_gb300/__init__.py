@@ -16,10 +16,10 @@ import ctypes
 from . import _lib
 from ._lib import (  # noqa: F401
     BF16, FP32, PREC_BF16, PREC_FP32, ROUTE_AUTO, ROUTE_GRAM, ROUTE_DIRECT, BUCKET_GRAM, BUCKET_DIRECT,
-    ENGINE_TC_BF16, ENGINE_SIMT_FP32, SCALE_ASPECT, SCALE_RMS, TIMER_NAMES, DmuonError,
+    ENGINE_TC_BF16, ENGINE_SIMT_FP32, SCALE_ASPECT, SCALE_RMS, TIMER_NAMES, ASSIGN_GREEDY, ASSIGN_EXACT, DmuonError,
 )
 
-__all__ = ["Muon", "dmuon_plan", "dmuon_step", "load"]
+__all__ = ["Muon", "dmuon_plan", "dmuon_step", "assign_owners", "load"]
 
 _DTYPES = {"bf16": BF16, "fp32": FP32}
 _PREC = {"bf16": PREC_BF16, "fp32": PREC_FP32}
@@ -82,6 +82,21 @@ def dmuon_step(h, params, grads, momenta, lr, beta, wd, ns_steps=5, stream=None)
     _lib.check(st, "dmuon_step")
 
 
+_ASSIGN = {"greedy": ASSIGN_GREEDY, "exact": ASSIGN_EXACT}
+
+
+def assign_owners(costs, ranks, method="greedy"):
+    """dmuon_assign_owners: (owner rank per matrix, makespan) for predicted costs."""
+    lib = _lib.load()
+    n = len(costs)
+    arr = (ctypes.c_double * max(n, 1))(*[float(c) for c in costs])
+    owner = (ctypes.c_int32 * max(n, 1))()
+    ms = ctypes.c_double()
+    _lib.check(lib.dmuon_assign_owners(arr, n, int(ranks), _ASSIGN[method], owner, ctypes.byref(ms)),
+               "dmuon_assign_owners")
+    return [int(owner[i]) for i in range(n)], ms.value
+
+
 class Muon:
     """One plan bound to a workspace: ``Muon(shapes).step(params, grads, moms, lr, beta, wd)``.
 
@@ -133,6 +148,12 @@ class Muon:
         out = (ctypes.c_double * 2)()
         _lib.check(self.lib.dmuon_plan_flops(self.handle, ns_steps, out), "dmuon_plan_flops")
         return out[0], out[1]
+
+    def matrix_flops(self, ns_steps=5):
+        """Per-matrix algorithmic FLOPs of one step, in the order of the shapes."""
+        out = (ctypes.c_double * max(len(self.shapes), 1))()
+        _lib.check(self.lib.dmuon_plan_matrix_flops(self.handle, ns_steps, out), "dmuon_plan_matrix_flops")
+        return [out[i] for i in range(len(self.shapes))]
 
     # ---- device
     def bind(self, workspace=None):

@@ -21,6 +21,7 @@ ERR_CUDA, ERR_DEVICE_TIMEOUT, ERR_UNSUPPORTED_DEVICE, ERR_WORKSPACE_TOO_SMALL = 
 MAX_NS_STEPS = 16
 TIMER_NAMES = ("momentum", "norm", "syrk", "ns", "final", "tc", "simt")
 BUF_X, BUF_RF, BUF_R_OPERAND = 0, 1, 2
+ASSIGN_GREEDY, ASSIGN_EXACT = 0, 1
 
 
 class Shape(ctypes.Structure):
@@ -62,6 +63,9 @@ SIGNATURES = {
     "dmuon_status_string": (c_char_p, [c_int]),
     "dmuon_debug_buffer": (c_int, [c_void_p, c_int64, c_int64, c_int32, POINTER(c_uint64), POINTER(c_int64),
                                    POINTER(c_int64), POINTER(c_int32)]),
+    "dmuon_assign_owners": (c_int, [POINTER(c_double), c_int64, c_int32, c_int32, POINTER(c_int32),
+                                    POINTER(c_double)]),
+    "dmuon_plan_matrix_flops": (c_int, [c_void_p, c_int32, POINTER(c_double)]),
     "dmuon_step_noalloc": (c_int, [c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_int32, c_float, c_float,
                                    c_float, c_int32, c_void_p]),
 }

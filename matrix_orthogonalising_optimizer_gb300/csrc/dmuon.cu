@@ -611,6 +611,19 @@ int dmuon_plan_flops(dmuon_handle_t h, int32_t ns_steps, double* out) {
     return DMUON_OK;
 }
 
+int dmuon_plan_matrix_flops(dmuon_handle_t h, int32_t ns_steps, double* flops) {
+    if (!h || !flops || ns_steps < 1 || ns_steps > DMUON_MAX_NS_STEPS)
+        return fail(DMUON_ERR_INVALID_ARG, "bad per-matrix flops query");
+    const double T = ns_steps;
+    for (const Bucket& b : h->buckets) {
+        const double m = static_cast<double>(b.m), n = static_cast<double>(b.n);
+        const double f = b.route == DMUON_BUCKET_GRAM ? 3.0 * m * m * n + (4.0 * T - 3.0) * m * m * m
+                                                      : T * (3.0 * m * m * n + m * m * m);
+        for (int64_t gi : b.members) flops[gi] = f;
+    }
+    return DMUON_OK;
+}
+
 size_t dmuon_workspace_bytes(dmuon_handle_t h) { return h ? static_cast<size_t>(h->ws_bytes) : 0; }
 
 int dmuon_bind_workspace(dmuon_handle_t h, void* dev_ptr, size_t bytes) {
