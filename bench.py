@@ -38,6 +38,7 @@ def parse_args():
     ap.add_argument("--config", default="c3", help="workload: c1..c5 (c3 is the measured one)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-adamw", action="store_true", help="skip the AdamW comparison step")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--budget-gb", type=float, default=0.0,
                     help="workspace budget per wave in GiB (0 = the configuration's own)")
@@ -299,6 +300,10 @@ def run_dmuon(args, cfg, world, rank, local):
     if not args.no_e2e:
         e2e = measure_e2e(muon, cfg, ws, gs, ms, args.e2e_steps, stream, world)
 
+    adamw = None
+    if not args.no_adamw:
+        adamw = measure_adamw(cfg, ws, gs, stream, args.steps, args.warmup, world, peaks, src)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(cfg)
@@ -323,8 +328,53 @@ def run_dmuon(args, cfg, world, rank, local):
             "step_frac_of_peak": flops_total / (ms_step / 1000.0) / 1e12 / peak,
             "stages_ms_per_step": stages, "launches_per_step": launches_per_step,
             "gpu_launches": int(launches), "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu,
+            "adamw": adamw,
+            "muon_over_adamw_step_time": ms_step / adamw["ms_per_step"] if adamw and "ms_per_step" in adamw
+            else None,
         }
         print(json.dumps(line), flush=True)
+
+
+def measure_adamw(cfg, ws, gs, stream, steps, warmup, world, peaks, src):
+    """The element-wise optimizer the pages compare against, on the same tensors: one
+    multi-tensor AdamW step (states in the parameters' dtype) timed like the Muon step.
+    Context for the Muon step time, not a second headline."""
+    import torch
+
+    from matrix_orthogonalising_optimizer_gb300 import adamw_step
+    need = 2 * sum(w.numel() * w.element_size() for w in ws)
+    free, _ = torch.cuda.mem_get_info()
+    if free < need + (4 << 30):
+        return {"skipped": f"states need {need / 2**30:.1f} GiB, {free / 2**30:.1f} GiB free"}
+    m = [torch.zeros_like(w) for w in ws]
+    v = [torch.zeros_like(w) for w in ws]
+    kw = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, wd=cfg.wd)
+    t = 0
+    for _ in range(max(warmup, 1)):
+        t += 1
+        adamw_step(ws, gs, m, v, step=t, stream=stream, **kw)
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        t += 1
+        adamw_step(ws, gs, m, v, step=t, stream=stream, **kw)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms_step = max_over_ranks(e0.elapsed_time(e1) / steps, world)
+    elems = sum(w.numel() for w in ws)
+    per_elem = 7 * ws[0].element_size()  # read W, g, m, v; write W, m, v
+    gbs = elems * per_elem / (ms_step / 1000.0) / 1e9
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    del m, v
+    torch.cuda.empty_cache()
+    return {"ms_per_step": ms_step, "matrices_per_s": replica_value(len(ws), world, ms_step),
+            "bytes_per_step": elems * per_elem, "achieved_gbs": gbs, "peak_gbs": hbm, "frac": gbs / hbm,
+            "peak_source": f"hbm_gbs of {src} peaks", "states_dtype": str(ws[0].dtype).replace("torch.", ""),
+            "hyper": kw}
 
 
 def measure_e2e(muon, cfg, ws, gs, ms, steps, stream, world):

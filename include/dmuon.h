@@ -260,6 +260,36 @@ int dmuon_assign_owners(const double* costs, int64_t count, int32_t ranks, int32
  * DMUON_OK or DMUON_ERR_INVALID_ARG. */
 int dmuon_plan_matrix_flops(dmuon_handle_t h, int32_t ns_steps, double* flops);
 
+/* ---- AdamW on the same tensors (comparison step) ------------------------
+ *
+ * The element-wise optimizer the pages measure DMuon against (technical
+ * summary, section 4: "+2 % per-step latency over AdamW"), so that the two
+ * optimizer steps can be timed on the same tensors.  Published AdamW with
+ * decoupled weight decay and bias correction; per element, in fp32 from the
+ * stored values, t = step:
+ *   m = beta1*m + (1-beta1)*g,  v = beta2*v + (1-beta2)*g^2
+ *   W = (1 - lr*wd)*W - lr/(1-beta1^t) * m / (sqrt(v)/sqrt(1-beta2^t) + eps)
+ * and W, m, v are stored back (round to nearest even).
+ *
+ * params, grads, exp_avgs, exp_avg_sqs: HOST arrays of `count` DEVICE
+ * pointers; tensor i holds numels[i] contiguous elements of dtypes[i]
+ * (DMUON_BF16 | DMUON_FP32) in all four arrays, each 16-byte aligned.
+ * params, exp_avgs and exp_avg_sqs are updated in place; grads are read.
+ * Asynchronous on `stream`; allocates nothing (the tensor table is passed as
+ * kernel parameters, 256 tensors per launch).  Every wait inside the kernel
+ * is bounded; dmuon_adamw_status() reports one that gave up.  Returns DMUON_OK,
+ * DMUON_ERR_INVALID_ARG (count, numel, step < 1, betas outside [0, 1),
+ * eps <= 0, NULL array), DMUON_ERR_UNSUPPORTED_DTYPE, DMUON_ERR_ALIGN or
+ * DMUON_ERR_CUDA. */
+int dmuon_adamw_step(void* const* params, const void* const* grads, void* const* exp_avgs,
+                     void* const* exp_avg_sqs, const int64_t* numels, const int32_t* dtypes, int64_t count,
+                     float lr, float beta1, float beta2, float eps, float wd, int64_t step, void* stream);
+/* Synchronous: DMUON_ERR_DEVICE_TIMEOUT if a wait inside an AdamW launch on
+ * the current device gave up (about 2 s; its tensors are then only partly
+ * updated) since the last call, else DMUON_OK; clears the flag.
+ * DMUON_ERR_CUDA if the flag cannot be read. */
+int dmuon_adamw_status(void);
+
 /* ---- one small matrix without device allocation ------------------------
  *
  * No counterpart in the paper: an addition for callers that cannot allocate

@@ -19,7 +19,7 @@ from ._lib import (  # noqa: F401
     ENGINE_TC_BF16, ENGINE_SIMT_FP32, SCALE_ASPECT, SCALE_RMS, TIMER_NAMES, ASSIGN_GREEDY, ASSIGN_EXACT, DmuonError,
 )
 
-__all__ = ["Muon", "dmuon_plan", "dmuon_step", "assign_owners", "load"]
+__all__ = ["Muon", "dmuon_plan", "dmuon_step", "assign_owners", "adamw_step", "load"]
 
 _DTYPES = {"bf16": BF16, "fp32": FP32}
 _PREC = {"bf16": PREC_BF16, "fp32": PREC_FP32}
@@ -83,6 +83,26 @@ def dmuon_step(h, params, grads, momenta, lr, beta, wd, ns_steps=5, stream=None)
 
 
 _ASSIGN = {"greedy": ASSIGN_GREEDY, "exact": ASSIGN_EXACT}
+
+
+def adamw_step(params, grads, exp_avgs, exp_avg_sqs, lr, beta1, beta2, eps, wd, step, stream=None):
+    """dmuon_adamw_step over lists of device tensors of one dtype each (bf16 or fp32)."""
+    import torch
+    lib = _lib.load()
+    n = len(params)
+    dts = {torch.bfloat16: BF16, torch.float32: FP32}
+
+    def ptrs(xs):
+        a = (ctypes.c_void_p * max(n, 1))()
+        for i, x in enumerate(xs):
+            a[i] = x.data_ptr()
+        return a
+
+    numel = (ctypes.c_int64 * max(n, 1))(*[p.numel() for p in params])
+    dtype = (ctypes.c_int32 * max(n, 1))(*[dts.get(p.dtype, -1) for p in params])
+    st = lib.dmuon_adamw_step(ptrs(params), ptrs(grads), ptrs(exp_avgs), ptrs(exp_avg_sqs), numel, dtype, n,
+                              lr, beta1, beta2, eps, wd, int(step), _stream_handle(stream))
+    _lib.check(st, "dmuon_adamw_step")
 
 
 def assign_owners(costs, ranks, method="greedy"):

@@ -66,6 +66,10 @@ SIGNATURES = {
     "dmuon_assign_owners": (c_int, [POINTER(c_double), c_int64, c_int32, c_int32, POINTER(c_int32),
                                     POINTER(c_double)]),
     "dmuon_plan_matrix_flops": (c_int, [c_void_p, c_int32, POINTER(c_double)]),
+    "dmuon_adamw_step": (c_int, [POINTER(c_void_p), POINTER(c_void_p), POINTER(c_void_p), POINTER(c_void_p),
+                                 POINTER(c_int64), POINTER(c_int32), c_int64, c_float, c_float, c_float, c_float,
+                                 c_float, c_int64, c_void_p]),
+    "dmuon_adamw_status": (c_int, []),
     "dmuon_step_noalloc": (c_int, [c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_int32, c_float, c_float,
                                    c_float, c_int32, c_void_p]),
 }

@@ -19,7 +19,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(HERE, "libdmuon.so")
-SOURCES = ["dmuon.cu", "momentum.cu", "gemm_tc.cu", "gemm_simt.cu", "noalloc.cu", "owners.cpp"]
+SOURCES = ["dmuon.cu", "momentum.cu", "gemm_tc.cu", "gemm_simt.cu", "noalloc.cu", "owners.cpp", "adamw.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 
