@@ -204,7 +204,17 @@ cudaError_t launch_momentum_pack(const MomentumArgs& a, cudaStream_t s) {
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 1) * 8;
+    // persistent blocks: exactly as many as fit at once (a grid of 8 per SM,
+    // 6 resident, ran its last 2 per SM as a second wave after the others)
+    static int per_sm = 0;
+    if (per_sm == 0) {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, momentum_pack_kernel, kMomThreads, 0) != cudaSuccess ||
+            n < 1)
+            n = 1;
+        per_sm = n;
+    }
+    const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 1) * per_sm;
     const int grid = static_cast<int>(a.total_tiles < cap ? a.total_tiles : cap);
     momentum_pack_kernel<<<grid, kMomThreads, 0, s>>>(a);
     return cudaGetLastError();
