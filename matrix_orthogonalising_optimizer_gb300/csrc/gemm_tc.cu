@@ -61,6 +61,10 @@ constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr int kTileRing = 4;
 constexpr int kTStageLd = 132;  // 128 W columns + 4 pad; 528-byte rows keep float4 reads aligned
 constexpr int kEpiWarps = (kTcThreads - 64) / 32;
+// epilogue warps come in sets of four (one per TMEM lane quarter); each set
+// takes an equal part of the 256 accumulator columns
+constexpr int kColParts = kEpiWarps / 4;
+static_assert(kEpiWarps % 4 == 0 && (kColParts == 1 || kColParts == 2), "4 or 8 epilogue warps");
 // readers of a tile slot: the 8 epilogue warps of each CTA, the leader's MMA
 // thread and the partner's producer
 constexpr uint32_t kTileReaders = kPair * kEpiWarps + 2;
@@ -794,6 +798,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
         uint32_t stage = 0, phase = 0;
         bool ok = true;
         int it = 0;
+        // shared-memory descriptors of stage 0; a stage, and a 16-deep K step
+        // inside it, only move the 14-bit start-address field (16-byte units),
+        // which stays below its top for every shared-memory address.  This
+        // thread alone feeds the pair's tensor cores and shares its scheduler
+        // with two epilogue warps: its loop is kept short.
+        const uint64_t a_desc0 = smem_desc(saddr(S.a[0]), 0, 1024);
+        const uint64_t b_desc0_k = smem_desc(saddr(S.b[0]), 0, 1024);
+        const uint64_t b_desc0_mn = smem_desc(saddr(S.b[0]), MN_BOX_BYTES, 1024);
         for (int k = 0; ok; ++k, ++it) {
             const int t = wait_tile(S.tile_full, S.tile_slot, k, L.status, total);
             release_tile(S.tile_empty, k);
@@ -808,21 +820,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
             const uint32_t d = tmem + static_cast<uint32_t>(buf * BN);
             const bool bmn = g->b_mn_major != 0;
             const uint32_t idesc = make_idesc(bmn);
+            const uint64_t b_desc0 = bmn ? b_desc0_mn : b_desc0_k;
+            const uint64_t b_kstep = bmn ? (UMMA_K * 128) >> 4 : (UMMA_K * 2) >> 4;
             for (int kb = 0; kb < nkb; ++kb) {
                 if (!mbar_wait(&S.full[stage], phase, L.status)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t a0 = saddr(S.a[stage]);
-                const uint32_t b0 = saddr(S.b[stage]);
+                const uint64_t ad0 = a_desc0 + static_cast<uint64_t>(stage) * (A_BYTES >> 4);
+                const uint64_t bd0 = b_desc0 + static_cast<uint64_t>(stage) * (B_BYTES >> 4);
 #pragma unroll
-                for (int kk = 0; kk < SLAB_K / UMMA_K; ++kk) {
-                    const uint64_t ad = smem_desc(a0 + kk * (UMMA_K * 2), 0, 1024);
-                    const uint64_t bd = bmn ? smem_desc(b0 + kk * (UMMA_K * 128), MN_BOX_BYTES, 1024)
-                                            : smem_desc(b0 + kk * (UMMA_K * 2), 0, 1024);
-                    umma_bf16(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
-                }
+                for (int kk = 0; kk < SLAB_K / UMMA_K; ++kk)
+                    umma_bf16(d, ad0 + kk * ((UMMA_K * 2) >> 4), bd0 + kk * b_kstep, idesc, (kb | kk) != 0 ? 1u : 0u);
                 umma_commit_mc(&S.empty[stage], kPairMask);
                 if (++stage == STAGES) {
                     stage = 0;
@@ -836,7 +846,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     } else if (warp >= 2) {
         // ------------------------------------------------ epilogue
         const int q = warp & 3;             // TMEM lane quarter this warp may access
-        const int half = (warp - 2) / 4;    // which 128 of the 256 columns
+        const int half = (warp - 2) / 4;    // which column part (of kColParts) of the 256 columns
         int it = 0;
         for (int k = 0;; ++k, ++it) {
             const int t = wait_tile(S.tile_full, S.tile_slot, k, L.status, total);
@@ -853,7 +863,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
             const int r = r0w + lane;
             const int row_last = tm * BM + BM - 1;
             // chunks of this warp that hold stored columns
-            constexpr int kChunks = (BN / 2) / CH;
+            constexpr int kChunks = (BN / kColParts) / CH;
             const int ch0 = half * kChunks;
             int nch = 0;
             for (int ch = ch0; ch < ch0 + kChunks; ++ch) {
