@@ -39,7 +39,7 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-adamw", action="store_true", help="skip the AdamW comparison step")
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--budget-gb", type=float, default=0.0,
                     help="workspace budget per wave in GiB (0 = the configuration's own)")
     return ap.parse_args()
@@ -379,30 +379,82 @@ def measure_adamw(cfg, ws, gs, stream, steps, warmup, world, peaks, src):
 
 def measure_e2e(muon, cfg, ws, gs, ms, steps, stream, world):
     """Same metric through the public API with host buffers: every step copies the
-    gradients host->device from pinned memory and reads the updated parameters back."""
+    gradients host->device from pinned memory and reads the updated parameters back.
+
+    The copies run on their own streams and overlap the compute: step i+1's gradients
+    go into a second device buffer while step i computes, and step i's parameters are
+    copied to a device snapshot (a device-to-device copy on the compute stream, so the
+    next step cannot update them first) and read back from it during step i+1.  The
+    timed region spans the first upload to the last read-back.  Without room for the
+    two extra copies of the set on the device, the copies run in line instead."""
     import torch
     host_g = [g.cpu().pin_memory() for g in gs]
     host_w = [torch.empty(w.shape, dtype=w.dtype, pin_memory=True) for w in ws]
     h2d = sum(g.numel() * g.element_size() for g in gs)
     d2h = sum(w.numel() * w.element_size() for w in ws)
     lr, beta, wd, T = cfg.lr, cfg.beta, cfg.wd, cfg.ns_steps
+    free, _ = torch.cuda.mem_get_info()
+    overlap = free > h2d + d2h + (4 << 30)
     torch.cuda.synchronize()
     barrier(world)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(steps):
-        for d, h in zip(gs, host_g):
-            d.copy_(h, non_blocking=True)
-        muon.step(ws, gs, ms, lr, beta, wd, T, stream)
-        for h, d in zip(host_w, ws):
-            h.copy_(d, non_blocking=True)
-    e1.record(stream)
+    if not overlap:
+        e0.record(stream)
+        for _ in range(steps):
+            for d, h in zip(gs, host_g):
+                d.copy_(h, non_blocking=True)
+            muon.step(ws, gs, ms, lr, beta, wd, T, stream)
+            for h, d in zip(host_w, ws):
+                h.copy_(d, non_blocking=True)
+        e1.record(stream)
+    else:
+        gbuf = [gs, [torch.empty_like(g) for g in gs]]
+        snap = [torch.empty_like(w) for w in ws]
+        s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+        ev = lambda: torch.cuda.Event()  # noqa: E731
+        uploaded, computed, snapped, read = [], [], [], []
+
+        def upload(i):
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(computed[i - 2])  # its buffer was read by step i-2
+                for d, h in zip(gbuf[i % 2], host_g):
+                    d.copy_(h, non_blocking=True)
+                uploaded.append(ev())
+                uploaded[-1].record(s_in)
+
+        e0.record(stream)
+        s_in.wait_event(e0)
+        upload(0)
+        for i in range(steps):
+            stream.wait_event(uploaded[i])
+            muon.step(ws, gbuf[i % 2], ms, lr, beta, wd, T, stream)
+            computed.append(ev())
+            computed[-1].record(stream)
+            if i + 1 < steps:
+                upload(i + 1)
+            if i >= 1:
+                stream.wait_event(read[i - 1])  # the snapshot is free again
+            for sn, w in zip(snap, ws):
+                sn.copy_(w, non_blocking=True)
+            snapped.append(ev())
+            snapped[-1].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(snapped[i])
+                for h, sn in zip(host_w, snap):
+                    h.copy_(sn, non_blocking=True)
+                read.append(ev())
+                read[-1].record(s_out)
+        stream.wait_event(read[-1])
+        e1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
     ms_step = max_over_ranks(e0.elapsed_time(e1) / steps, world)
     return {"value": replica_value(len(cfg.shapes), world, ms_step), "unit": "matrices/s",
-            "ms_per_step": ms_step, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "ms_per_step": ms_step, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "copies": "overlapped with compute (double-buffered gradients, device snapshot of the parameters)"
+            if overlap else "in line"}
 
 
 def main():
