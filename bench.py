@@ -39,6 +39,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-adamw", action="store_true", help="skip the AdamW comparison step")
+    ap.add_argument("--owners", type=int, default=8,
+                    help="owner-model leg: ranks D the set is split over (0 = skip)")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--budget-gb", type=float, default=0.0,
                     help="workspace budget per wave in GiB (0 = the configuration's own)")
@@ -300,6 +302,10 @@ def run_dmuon(args, cfg, world, rank, local):
     if not args.no_e2e:
         e2e = measure_e2e(muon, cfg, ws, gs, ms, args.e2e_steps, stream, world)
 
+    owners = None
+    if args.owners > 0 and world == 1:
+        owners = measure_owner_model(cfg, ws, gs, ms, stream, args.owners, ms_step)
+
     adamw = None
     if not args.no_adamw:
         adamw = measure_adamw(cfg, ws, gs, stream, args.steps, args.warmup, world, peaks, src)
@@ -328,11 +334,67 @@ def run_dmuon(args, cfg, world, rank, local):
             "step_frac_of_peak": flops_total / (ms_step / 1000.0) / 1e12 / peak,
             "stages_ms_per_step": stages, "launches_per_step": launches_per_step,
             "gpu_launches": int(launches), "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu,
-            "adamw": adamw,
+            "adamw": adamw, "owner_model": owners,
             "muon_over_adamw_step_time": ms_step / adamw["ms_per_step"] if adamw and "ms_per_step" in adamw
             else None,
         }
         print(json.dumps(line), flush=True)
+
+
+def _time_subset(cfg, idx, ws, gs, ms, stream, warmup=2, steps=3):
+    """ms per step of the Muon step restricted to the matrices `idx` (own plan and workspace)."""
+    import torch
+
+    from matrix_orthogonalising_optimizer_gb300 import Muon
+    dt = 0 if cfg.dtype == "bf16" else 1
+    sub = Muon([(cfg.shapes[i][0], cfg.shapes[i][1], dt) for i in idx], precision=cfg.precision).bind()
+    w, g, m = [ws[i] for i in idx], [gs[i] for i in idx], [ms[i] for i in idx]
+    for _ in range(warmup):
+        sub.step(w, g, m, cfg.lr, cfg.beta, cfg.wd, cfg.ns_steps, stream)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        sub.step(w, g, m, cfg.lr, cfg.beta, cfg.wd, cfg.ns_steps, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    status = sub.device_status(stream)
+    del sub
+    torch.cuda.empty_cache()
+    if status != 0:
+        raise RuntimeError("device status set in the owner-model leg")
+    return e0.elapsed_time(e1) / steps
+
+
+def measure_owner_model(cfg, ws, gs, ms, stream, ranks, redundant_ms):
+    """The pages' owner-centric execution at one GPU (DMuon summary, sections 2.1 and 2.3).
+
+    Without owners every rank runs the whole set's update (the replicated
+    step timed above).  With owners each matrix is updated once, by the rank
+    that owns it; owners are assigned from measured costs (each bucket's step
+    timed alone, divided by its count), and the step of each rank's share is
+    timed here one rank after another.  Reports the slowest rank against the
+    replicated step."""
+    from matrix_orthogonalising_optimizer_gb300 import Muon, assign_owners
+    dt = 0 if cfg.dtype == "bf16" else 1
+    plan = Muon([(r, c, dt) for r, c in cfg.shapes], precision=cfg.precision)
+    cost = [0.0] * len(cfg.shapes)
+    per_bucket = []
+    for b in plan.buckets():
+        t = _time_subset(cfg, b["members"], ws, gs, ms, stream)
+        per_bucket.append({"m": b["m"], "n": b["n"], "count": len(b["members"]), "ms": t})
+        for i in b["members"]:
+            cost[i] = t / len(b["members"])
+    owner, predicted = assign_owners(cost, ranks, "greedy")
+    flops_owner, flops_pred = assign_owners(plan.matrix_flops(cfg.ns_steps), ranks, "greedy")
+    rank_ms = [_time_subset(cfg, [i for i in range(len(owner)) if owner[i] == r], ws, gs, ms, stream)
+               if r in owner else 0.0 for r in range(ranks)]
+    slowest = max(rank_ms)
+    return {"ranks": ranks, "cost_model": "measured: each bucket's step alone / its count",
+            "bucket_ms": per_bucket, "predicted_makespan_ms": predicted, "rank_ms": rank_ms,
+            "slowest_rank_ms": slowest, "replicated_ms": redundant_ms,
+            "speedup_over_replicated": redundant_ms / slowest if slowest > 0 else None,
+            "owners_same_as_flop_model": owner == flops_owner}
 
 
 def measure_adamw(cfg, ws, gs, stream, steps, warmup, world, peaks, src):
