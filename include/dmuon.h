@@ -99,7 +99,9 @@ typedef struct {
     int64_t rows;     /* >= 1 */
     int64_t cols;     /* >= 1 */
     int32_t dtype;    /* DMUON_BF16 | DMUON_FP32 */
-    int32_t reserved; /* must be 0 */
+    int32_t route;    /* this matrix's route rule: 0 (DMUON_ROUTE_AUTO) = the plan's
+                         options->route; DMUON_ROUTE_GRAM or DMUON_ROUTE_DIRECT override it
+                         (e.g. from a measured per-bucket choice) */
 } dmuon_shape_t;
 
 /* Zero-initialised options give the defaults noted on each field. */
@@ -130,13 +132,16 @@ typedef struct {
 
 /* Shape-bucketing planner.  Each shape is canonicalised to (m, n, transposed)
  * with m = min(rows, cols), n = max(rows, cols), transposed = rows > cols
- * (tall matrices are packed transposed).  Buckets are keyed (dtype, m, n),
- * ordered by that key ascending; matrices keep their input order inside a
- * bucket.  Buckets are then packed, in bucket order, into waves whose
+ * (tall matrices are packed transposed), and its route resolved: the shape's
+ * own rule, else options->route; AUTO gives Gram when n >= 3m or m <=
+ * small_m, else direct; FP32 precision gives Gram unless the rule is DIRECT.
+ * Buckets are keyed (dtype, m, n, route), ordered by that key ascending
+ * (DMUON_BUCKET_GRAM before DMUON_BUCKET_DIRECT); matrices keep their input
+ * order inside a bucket.  Buckets are then packed, in bucket order, into waves whose
  * workspace fits options->workspace_budget, splitting a bucket where needed.
  * Returns NULL on error (message in dmuon_last_error): count < 1, a NULL
  * pointer, a dimension outside [1, DMUON_MAX_DIM], rows*cols >=
- * DMUON_MAX_ELEMS, an unknown dtype, a non-zero reserved field, bad options,
+ * DMUON_MAX_ELEMS, an unknown dtype, an unknown shape route, bad options,
  * or a budget smaller than one matrix. */
 dmuon_handle_t dmuon_plan(const dmuon_shape_t* shapes, int64_t count);
 dmuon_handle_t dmuon_plan_ex(const dmuon_shape_t* shapes, int64_t count,

@@ -42,14 +42,16 @@ def _stream_handle(stream):
 
 def dmuon_plan(shapes, dtype="bf16", precision="bf16", route="auto", coeffs=None, eps=0.0,
                scale_rule="aspect", nesterov=True, small_m=0, workspace_budget=0):
-    """dmuon_plan_ex: shapes is a list of (rows, cols) or (rows, cols, dtype)."""
+    """dmuon_plan_ex: shapes is a list of (rows, cols[, dtype[, route]]); a shape's route
+    ("auto" / 0 = the plan's ``route``, "gram", "direct") overrides the plan's rule."""
     lib = _lib.load()
     arr = (_lib.Shape * len(shapes))()
     for i, s in enumerate(shapes):
         dt = s[2] if len(s) > 2 else dtype
         arr[i].rows, arr[i].cols = int(s[0]), int(s[1])
         arr[i].dtype = _DTYPES[dt] if isinstance(dt, str) else int(dt)
-        arr[i].reserved = 0
+        rt = s[3] if len(s) > 3 else 0
+        arr[i].route = _ROUTES[rt] if isinstance(rt, str) else int(rt)
     opt = _lib.Options()
     opt.precision = _PREC[precision]
     opt.route = _ROUTES[route]

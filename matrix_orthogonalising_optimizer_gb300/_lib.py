@@ -25,7 +25,7 @@ ASSIGN_GREEDY, ASSIGN_EXACT = 0, 1
 
 
 class Shape(ctypes.Structure):
-    _fields_ = [("rows", c_int64), ("cols", c_int64), ("dtype", c_int32), ("reserved", c_int32)]
+    _fields_ = [("rows", c_int64), ("cols", c_int64), ("dtype", c_int32), ("route", c_int32)]
 
 
 class Options(ctypes.Structure):

@@ -402,11 +402,19 @@ dmuon_handle_t dmuon_plan_ex(const dmuon_shape_t* shapes, int64_t count, const d
     h->count = count;
     h->shapes.assign(shapes, shapes + count);
 
-    std::map<std::tuple<int32_t, int64_t, int64_t>, std::vector<int64_t>> keyed;
+    // route of one matrix: its own rule, else the plan's; AUTO by shape
+    auto resolve = [&](int32_t rule, int64_t m, int64_t n) {
+        const bool small = h->small_m > 0 && m <= h->small_m;
+        if (h->precision == DMUON_PREC_FP32) return rule == DMUON_ROUTE_DIRECT ? DMUON_BUCKET_DIRECT : DMUON_BUCKET_GRAM;
+        if (rule == DMUON_ROUTE_GRAM) return DMUON_BUCKET_GRAM;
+        if (rule == DMUON_ROUTE_DIRECT) return DMUON_BUCKET_DIRECT;
+        return (n >= 3 * m || small) ? DMUON_BUCKET_GRAM : DMUON_BUCKET_DIRECT;
+    };
+    std::map<std::tuple<int32_t, int64_t, int64_t, int32_t>, std::vector<int64_t>> keyed;
     for (int64_t i = 0; i < count; ++i) {
         const dmuon_shape_t& s = shapes[i];
         if (s.rows < 1 || s.cols < 1 || s.rows > DMUON_MAX_DIM || s.cols > DMUON_MAX_DIM ||
-            s.rows * s.cols >= DMUON_MAX_ELEMS || s.reserved != 0) {
+            s.rows * s.cols >= DMUON_MAX_ELEMS || s.route < DMUON_ROUTE_AUTO || s.route > DMUON_ROUTE_DIRECT) {
             fail(DMUON_ERR_INVALID_ARG, "shape " + std::to_string(i) + " out of range");
             delete h;
             return nullptr;
@@ -416,7 +424,9 @@ dmuon_handle_t dmuon_plan_ex(const dmuon_shape_t* shapes, int64_t count, const d
             delete h;
             return nullptr;
         }
-        keyed[std::make_tuple(s.dtype, std::min(s.rows, s.cols), std::max(s.rows, s.cols))].push_back(i);
+        const int64_t m = std::min(s.rows, s.cols), n = std::max(s.rows, s.cols);
+        const int32_t rule = s.route != DMUON_ROUTE_AUTO ? s.route : h->route_rule;
+        keyed[std::make_tuple(s.dtype, m, n, static_cast<int32_t>(resolve(rule, m, n)))].push_back(i);
     }
     int64_t slot = 0;
     for (auto& kv : keyed) {
@@ -426,14 +436,7 @@ dmuon_handle_t dmuon_plan_ex(const dmuon_shape_t* shapes, int64_t count, const d
         b.n = std::get<2>(kv.first);
         b.members = kv.second;
         const bool small = h->small_m > 0 && b.m <= h->small_m;
-        if (h->precision == DMUON_PREC_FP32)
-            b.route = h->route_rule == DMUON_ROUTE_DIRECT ? DMUON_BUCKET_DIRECT : DMUON_BUCKET_GRAM;
-        else if (h->route_rule == DMUON_ROUTE_GRAM)
-            b.route = DMUON_BUCKET_GRAM;
-        else if (h->route_rule == DMUON_ROUTE_DIRECT)
-            b.route = DMUON_BUCKET_DIRECT;
-        else
-            b.route = (b.n >= 3 * b.m || small) ? DMUON_BUCKET_GRAM : DMUON_BUCKET_DIRECT;
+        b.route = std::get<3>(kv.first);
         if (h->precision == DMUON_PREC_FP32) b.engine = DMUON_ENGINE_SIMT_FP32;
         else if (b.route == DMUON_BUCKET_GRAM && small) b.engine = DMUON_ENGINE_SIMT_FP32;
         else b.engine = DMUON_ENGINE_TC_BF16;

@@ -9,9 +9,11 @@ C ABI header ``include/dmuon.h`` states for ``dmuon_plan``:
 
 * canonical shape: m = min(rows, cols), n = max(rows, cols); tall matrices
   (rows > cols) are packed transposed;
-* buckets keyed (dtype, m, n), ascending; input order inside a bucket;
-* route per bucket: FP32 precision -> Gram unless forced; AUTO -> Gram when
+* input order inside a bucket;
+* route per matrix: its own rule if the shape gives one, else the plan's;
+  FP32 precision -> Gram unless the rule is DIRECT; AUTO -> Gram when
   n >= 3m or m <= small_m, else direct;
+* buckets keyed (dtype, m, n, route), ascending;
 * m x m engine: FP32 precision -> fp32 FFMA; BF16 precision -> fp32 FFMA for
   Gram buckets with m <= small_m, tensor cores otherwise;
 * per-matrix workspace bytes: the sum of the per-matrix buffers below, each
@@ -57,28 +59,31 @@ def per_matrix_bytes(m: int, n: int, precision: int, route: int, engine: int) ->
 
 def plan_buckets(shapes, precision: int = PREC_BF16, route: int = ROUTE_AUTO,
                  small_m: int = 0, budget: int = 0):
-    """shapes: list of (rows, cols, dtype).  Returns (buckets, waves).
+    """shapes: list of (rows, cols, dtype[, route]).  Returns (buckets, waves).
 
     buckets: list of dicts with dtype, m, n, members (input indices), route,
     engine, per_matrix_bytes.  waves: list of lists of (bucket, start, count).
     """
     if small_m == 0:
         small_m = 256
+    def resolve(rule, m, n):
+        if precision == PREC_FP32:
+            return BUCKET_DIRECT if rule == ROUTE_DIRECT else BUCKET_GRAM
+        if rule == ROUTE_GRAM:
+            return BUCKET_GRAM
+        if rule == ROUTE_DIRECT:
+            return BUCKET_DIRECT
+        return BUCKET_GRAM if (n >= 3 * m or (small_m > 0 and m <= small_m)) else BUCKET_DIRECT
+
     keyed = {}
-    for idx, (rows, cols, dtype) in enumerate(shapes):
+    for idx, shp in enumerate(shapes):
+        rows, cols, dtype = shp[:3]
+        own = shp[3] if len(shp) > 3 else ROUTE_AUTO
         m, n = min(rows, cols), max(rows, cols)
-        keyed.setdefault((dtype, m, n), []).append(idx)
+        keyed.setdefault((dtype, m, n, resolve(own if own != ROUTE_AUTO else route, m, n)), []).append(idx)
     buckets = []
     for key in sorted(keyed):
-        dtype, m, n = key
-        if precision == PREC_FP32:
-            r = BUCKET_DIRECT if route == ROUTE_DIRECT else BUCKET_GRAM
-        elif route == ROUTE_GRAM:
-            r = BUCKET_GRAM
-        elif route == ROUTE_DIRECT:
-            r = BUCKET_DIRECT
-        else:
-            r = BUCKET_GRAM if (n >= 3 * m or (small_m > 0 and m <= small_m)) else BUCKET_DIRECT
+        dtype, m, n, r = key
         if precision == PREC_FP32:
             eng = ENGINE_SIMT_FP32
         elif r == BUCKET_GRAM and small_m > 0 and m <= small_m:

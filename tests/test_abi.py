@@ -73,6 +73,27 @@ def test_planner_matches_oracle_random(seed):
         _check_same(shapes, budget=big * mult + 12345)
 
 
+@pytest.mark.parametrize("seed", range(4))
+def test_planner_per_shape_routes_match_oracle(seed):
+    # a shape's own route overrides the plan's rule; equal shapes with
+    # different routes land in different buckets (Gram before direct)
+    g = torch.Generator().manual_seed(100 + seed)
+    base = [(r, c, int(torch.randint(0, 2, (1,), generator=g))) for r, c in
+            workloads.random_shapes(seed, 80, 1, 600)]
+    base = base + base[:30]
+    shapes = [s + (int(torch.randint(0, 3, (1,), generator=g)),) for s in base]
+    for prec in ("bf16", "fp32"):
+        for route in ("auto", "gram", "direct"):
+            _check_same(shapes, precision=prec, route=route)
+    b, _ = oplan.plan_buckets(shapes)
+    _check_same(shapes, budget=max(x["per_matrix_bytes"] for x in b) * 5 + 999)
+    # forcing a route per shape equals forcing it for the plan
+    for r, name in ((1, "gram"), (2, "direct")):
+        _, got, _ = _lib_plan([s[:3] + (r,) for s in base])
+        _, want, _ = _lib_plan(base, route=name)
+        assert got == want
+
+
 def test_planner_is_order_independent_up_to_members():
     shapes = [(r, c, 0) for r, c in workloads.random_shapes(3, 80, 1, 300)]
     perm = list(reversed(range(len(shapes))))
@@ -84,9 +105,9 @@ def test_planner_is_order_independent_up_to_members():
 
 
 def test_plan_errors(lib):
-    def plan(rows, cols, dtype=0, reserved=0, **kw):
+    def plan(rows, cols, dtype=0, shape_route=0, **kw):
         arr = (_lib.Shape * 1)()
-        arr[0].rows, arr[0].cols, arr[0].dtype, arr[0].reserved = rows, cols, dtype, reserved
+        arr[0].rows, arr[0].cols, arr[0].dtype, arr[0].route = rows, cols, dtype, shape_route
         opt = _lib.Options()
         for k, v in kw.items():
             setattr(opt, k, v)
@@ -94,7 +115,8 @@ def test_plan_errors(lib):
 
     assert plan(4, 4)
     for bad in [dict(rows=0, cols=4), dict(rows=4, cols=-1), dict(rows=1 << 21, cols=1),
-                dict(rows=1 << 20, cols=1 << 20), dict(rows=4, cols=4, dtype=7), dict(rows=4, cols=4, reserved=1),
+                dict(rows=1 << 20, cols=1 << 20), dict(rows=4, cols=4, dtype=7), dict(rows=4, cols=4, shape_route=3),
+                dict(rows=4, cols=4, shape_route=-1),
                 dict(rows=4, cols=4, precision=9), dict(rows=4, cols=4, route=5), dict(rows=4, cols=4, eps=-1.0),
                 dict(rows=4, cols=4, scale_rule=3), dict(rows=4, cols=4, no_nesterov=2)]:
         assert not plan(**bad), bad
