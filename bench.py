@@ -39,6 +39,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-adamw", action="store_true", help="skip the AdamW comparison step")
+    ap.add_argument("--routes", choices=["auto", "tuned"], default="auto",
+                    help="tuned: time Gram against direct per bucket first (autotune cache), plan with the faster")
     ap.add_argument("--owners", type=int, default=8,
                     help="owner-model leg: ranks D the set is split over (0 = skip)")
     ap.add_argument("--e2e-steps", type=int, default=10)
@@ -251,7 +253,13 @@ def run_dmuon(args, cfg, world, rank, local):
     _lib.load(build_if_missing=True)
     dt = 0 if cfg.dtype == "bf16" else 1
     budget = int((args.budget_gb or cfg.budget_gb) * (1 << 30))
-    muon = Muon([(r, c, dt) for r, c in cfg.shapes], precision=cfg.precision, workspace_budget=budget).bind()
+    shapes = [(r, c, dt) for r, c in cfg.shapes]
+    if args.routes == "tuned":
+        from matrix_orthogonalising_optimizer_gb300.autotune import autotune_routes
+        routes, _ = autotune_routes([(r, c, cfg.dtype) for r, c in cfg.shapes], precision=cfg.precision,
+                                    ns_steps=cfg.ns_steps)
+        shapes = [s + (rt,) for s, rt in zip(shapes, routes)]
+    muon = Muon(shapes, precision=cfg.precision, workspace_budget=budget).bind()
     ws, gs, ms = workloads.make_set(cfg, "cuda")
     torch.cuda.synchronize()
     lr, beta, wd, T = cfg.lr, cfg.beta, cfg.wd, cfg.ns_steps
@@ -323,7 +331,7 @@ def run_dmuon(args, cfg, world, rank, local):
             "config": {"workload": workloads_name(cfg), "matrices": n_mat, "ns_steps": T,
                        "elements": workloads.total_elements(cfg), "lr": lr, "beta": beta, "wd": wd,
                        "l2": "inputs larger than L2 (resident in HBM)",
-                       "parallelism": "replicas" if world > 1 else "single GPU"},
+                       "parallelism": "replicas" if world > 1 else "single GPU", "routes": args.routes},
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak,
                          "traffic": measured_traffic() if args.config == "c3" else None,
