@@ -10,6 +10,9 @@ does not reuse the oracle's own arithmetic:
 * Gram-space and direct NS agree (the identity behind the summary's
   section 2.2 "Gram Newton-Schulz iteration");
 * an orthonormal input is mapped to f^5(m^-1/2) times itself;
+* the golden table tests/golden/quintic_map.txt (f^k(s) iterated in exact
+  rational arithmetic by tests/golden/make_quintic_map.py) on diagonal and
+  rotated inputs;
 * zero, rank-1, scaled and transposed inputs;
 * bf16 round-to-nearest-even against hand-made halfway cases and torch;
 * the planner rules against hand-worked bucket lists.
@@ -314,3 +317,39 @@ def test_plan_fp32_and_forced_routes():
     b, _ = oplan.plan_buckets([(600, 700, 0), (200, 210, 0)])
     assert [(x["route"], x["engine"]) for x in b] == [(oplan.BUCKET_GRAM, oplan.ENGINE_SIMT_FP32),
                                                       (oplan.BUCKET_DIRECT, oplan.ENGINE_TC_BF16)]
+
+
+def _quintic_table():
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", "quintic_map.txt")
+    rows = []
+    for line in open(path):
+        if line.startswith("#") or not line.strip():
+            continue
+        parts = line.split()
+        rows.append((float(parts[0]), [float(x) for x in parts[1:]]))
+    return rows
+
+
+@pytest.mark.parametrize("route", ["direct", "gram"])
+def test_ns_singular_values_follow_the_exact_scalar_map(route):
+    # golden table: f^k(s) iterated in exact rational arithmetic by
+    # tests/golden/make_quintic_map.py.  Diagonal input: the singular values
+    # are the starting values, and k steps map each one to f^k(s) exactly
+    # (up to fp64 rounding).  Rotated input: the same singular values.
+    rows = _quintic_table()
+    s = np.array([r[0] for r in rows])
+    m, n = len(s), len(s) + 7
+    rng = np.random.default_rng(5)
+    u, _ = np.linalg.qr(rng.standard_normal((m, m)))
+    v, _ = np.linalg.qr(rng.standard_normal((n, n)))
+    ns = oracle.ns_direct if route == "direct" else oracle.ns_gram
+    for k in range(1, 7):
+        want = np.array([r[1][k - 1] for r in rows])
+        x0 = np.zeros((m, n))
+        x0[np.arange(m), np.arange(m)] = s
+        out = ns(x0, k)
+        np.testing.assert_allclose(np.diag(out[:, :m]), want, rtol=1e-12, atol=1e-15)
+        assert np.abs(out[:, m:]).max() == 0.0
+        rot = ns(u @ x0 @ v.T, k)
+        np.testing.assert_allclose(np.sort(np.linalg.svd(rot, compute_uv=False)), np.sort(want), rtol=1e-10)
