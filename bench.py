@@ -447,7 +447,7 @@ def measure_adamw(cfg, ws, gs, stream, steps, warmup, world, peaks, src):
             "hyper": kw}
 
 
-def measure_e2e(muon, cfg, ws, gs, ms, steps, stream, world):
+def measure_e2e(muon, cfg, ws, gs, ms, steps, stream, world, overlap=None, host_out=None):
     """Same metric through the public API with host buffers: every step copies the
     gradients host->device from pinned memory and reads the updated parameters back.
 
@@ -464,7 +464,8 @@ def measure_e2e(muon, cfg, ws, gs, ms, steps, stream, world):
     d2h = sum(w.numel() * w.element_size() for w in ws)
     lr, beta, wd, T = cfg.lr, cfg.beta, cfg.wd, cfg.ns_steps
     free, _ = torch.cuda.mem_get_info()
-    overlap = free > h2d + d2h + (4 << 30)
+    if overlap is None:
+        overlap = free > h2d + d2h + (4 << 30)
     torch.cuda.synchronize()
     barrier(world)
     e0 = torch.cuda.Event(enable_timing=True)
@@ -521,6 +522,8 @@ def measure_e2e(muon, cfg, ws, gs, ms, steps, stream, world):
     torch.cuda.synchronize()
     barrier(world)
     ms_step = max_over_ranks(e0.elapsed_time(e1) / steps, world)
+    if host_out is not None:
+        host_out.extend(host_w)
     return {"value": replica_value(len(cfg.shapes), world, ms_step), "unit": "matrices/s",
             "ms_per_step": ms_step, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "copies": "overlapped with compute (double-buffered gradients, device snapshot of the parameters)"
