@@ -37,6 +37,9 @@
  *    NULL = legacy default stream).  It allocates nothing and never
  *    synchronises the host, except that a change of the pointer set since the
  *    previous step uploads the new pointer table with one pageable copy.
+ *    With the same pointer set as the previous call it issues only stream
+ *    work (memsets and kernel launches), so such a call can be captured in a
+ *    CUDA graph and replayed (timers off).
  *  - Errors are negative status codes; dmuon_last_error() gives the message
  *    of the calling thread's last failure.  A handle must not be used on two
  *    streams at once.

@@ -298,3 +298,37 @@ def test_c5_large_layers_full_size_sampled():
         pytest.skip(f"needs about 280 GB free, {free / 1e9:.0f} GB free")
     # 8192^2 (direct) and 28672x8192 (tall, Gram)
     _full_size_sampled("c5", [0, 1])
+
+
+def test_step_replays_from_a_cuda_graph():
+    # After one eager step has uploaded the pointer table, dmuon_step issues
+    # only stream work (memsets and launches): it can be captured once and
+    # replayed, with bitwise the same results as eager steps.
+    from matrix_orthogonalising_optimizer_gb300 import Muon
+    shapes = [(320, 704), (704, 320), (300, 300), (64, 256), (1100, 520)]
+    inputs = make_inputs(shapes, "bf16", 41)
+    state = []
+    for _ in range(2):
+        muon = Muon([(r, c, 0) for r, c in shapes]).bind()
+        ws = [w.cuda() for w, _, _ in inputs]
+        gs = [g.cuda() for _, g, _ in inputs]
+        ms = [m.cuda().clone() for _, _, m in inputs]
+        state.append((muon, ws, gs, ms))
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for muon, ws, gs, ms in state:
+            muon.step(ws, gs, ms, LR, BETA, WD, 5, side)
+        muon, ws, gs, ms = state[1]
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=side):
+            muon.step(ws, gs, ms, LR, BETA, WD, 5, side)
+    torch.cuda.current_stream().wait_stream(side)
+    e_muon, e_ws, e_gs, e_ms = state[0]
+    for _ in range(3):
+        e_muon.step(e_ws, e_gs, e_ms, LR, BETA, WD, 5)
+        graph.replay()
+    torch.cuda.synchronize()
+    assert e_muon.device_status() == 0 and state[1][0].device_status() == 0
+    for a, b in zip(e_ws + e_ms, ws + ms):
+        assert torch.equal(a, b)
