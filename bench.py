@@ -453,10 +453,10 @@ def measure_e2e(muon, cfg, ws, gs, ms, steps, stream, world, overlap=None, host_
 
     The copies run on their own streams and overlap the compute: step i+1's gradients
     go into a second device buffer while step i computes, and step i's parameters are
-    copied to a device snapshot (a device-to-device copy on the compute stream, so the
-    next step cannot update them first) and read back from it during step i+1.  The
-    timed region spans the first upload to the last read-back.  Without room for the
-    two extra copies of the set on the device, the copies run in line instead."""
+    read back while step i+1 runs its momentum and Newton-Schulz phases; step i+1 waits
+    for that read only before its first parameter write (dmuon_step_ex's params_ready
+    event).  The timed region spans the first upload to the last read-back.  Without
+    room for a second copy of the gradients on the device the copies run in line."""
     import torch
     host_g = [g.cpu().pin_memory() for g in gs]
     host_w = [torch.empty(w.shape, dtype=w.dtype, pin_memory=True) for w in ws]
@@ -465,7 +465,7 @@ def measure_e2e(muon, cfg, ws, gs, ms, steps, stream, world, overlap=None, host_
     lr, beta, wd, T = cfg.lr, cfg.beta, cfg.wd, cfg.ns_steps
     free, _ = torch.cuda.mem_get_info()
     if overlap is None:
-        overlap = free > h2d + d2h + (4 << 30)
+        overlap = free > h2d + (4 << 30)
     torch.cuda.synchronize()
     barrier(world)
     e0 = torch.cuda.Event(enable_timing=True)
@@ -481,10 +481,9 @@ def measure_e2e(muon, cfg, ws, gs, ms, steps, stream, world, overlap=None, host_
         e1.record(stream)
     else:
         gbuf = [gs, [torch.empty_like(g) for g in gs]]
-        snap = [torch.empty_like(w) for w in ws]
         s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
         ev = lambda: torch.cuda.Event()  # noqa: E731
-        uploaded, computed, snapped, read = [], [], [], []
+        uploaded, computed, read = [], [], []
 
         def upload(i):
             with torch.cuda.stream(s_in):
@@ -500,21 +499,15 @@ def measure_e2e(muon, cfg, ws, gs, ms, steps, stream, world, overlap=None, host_
         upload(0)
         for i in range(steps):
             stream.wait_event(uploaded[i])
-            muon.step(ws, gbuf[i % 2], ms, lr, beta, wd, T, stream)
+            muon.step(ws, gbuf[i % 2], ms, lr, beta, wd, T, stream, params_ready=read[i - 1] if i else None)
             computed.append(ev())
             computed[-1].record(stream)
             if i + 1 < steps:
                 upload(i + 1)
-            if i >= 1:
-                stream.wait_event(read[i - 1])  # the snapshot is free again
-            for sn, w in zip(snap, ws):
-                sn.copy_(w, non_blocking=True)
-            snapped.append(ev())
-            snapped[-1].record(stream)
             with torch.cuda.stream(s_out):
-                s_out.wait_event(snapped[i])
-                for h, sn in zip(host_w, snap):
-                    h.copy_(sn, non_blocking=True)
+                s_out.wait_event(computed[i])
+                for h, w in zip(host_w, ws):
+                    h.copy_(w, non_blocking=True)
                 read.append(ev())
                 read[-1].record(s_out)
         stream.wait_event(read[-1])
@@ -526,7 +519,7 @@ def measure_e2e(muon, cfg, ws, gs, ms, steps, stream, world, overlap=None, host_
         host_out.extend(host_w)
     return {"value": replica_value(len(cfg.shapes), world, ms_step), "unit": "matrices/s",
             "ms_per_step": ms_step, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "copies": "overlapped with compute (double-buffered gradients, device snapshot of the parameters)"
+            "copies": "overlapped with compute (double-buffered gradients; parameters read back during the next step's earlier phases)"
             if overlap else "in line"}
 
 

@@ -189,6 +189,17 @@ int dmuon_step(dmuon_handle_t h, void* const* params, const void* const* grads,
                void* const* momenta, float lr, float beta, float wd,
                int32_t ns_steps, void* stream);
 
+/* dmuon_step, with one more ordering point: if params_ready (a cudaEvent_t
+ * passed as void*) is not NULL, `stream` waits for it right before the first
+ * launch that writes the parameters -- the final product of the first wave;
+ * the momentum, normalisation and Newton-Schulz launches before it do not
+ * wait.  A caller still reading the previous step's parameters (e.g. copying
+ * them to the host on another stream) records params_ready when done and so
+ * overlaps that read with this step's earlier phases.  Same return codes as
+ * dmuon_step. */
+int dmuon_step_ex(dmuon_handle_t h, void* const* params, const void* const* grads, void* const* momenta,
+                  float lr, float beta, float wd, int32_t ns_steps, void* stream, void* params_ready);
+
 /* Synchronises `stream`, returns the device status word (DMUON_OK or
  * DMUON_ERR_DEVICE_TIMEOUT) and clears it. */
 int dmuon_device_status(dmuon_handle_t h, void* stream);

@@ -68,8 +68,9 @@ def dmuon_plan(shapes, dtype="bf16", precision="bf16", route="auto", coeffs=None
     return h
 
 
-def dmuon_step(h, params, grads, momenta, lr, beta, wd, ns_steps=5, stream=None):
-    """dmuon_step over lists of device tensors (or raw device pointers)."""
+def dmuon_step(h, params, grads, momenta, lr, beta, wd, ns_steps=5, stream=None, params_ready=None):
+    """dmuon_step over lists of device tensors (or raw device pointers); with ``params_ready``
+    (a recorded torch.cuda.Event) dmuon_step_ex: the first parameter write waits for it."""
     lib = _lib.load()
     n = len(params)
 
@@ -79,8 +80,13 @@ def dmuon_step(h, params, grads, momenta, lr, beta, wd, ns_steps=5, stream=None)
             a[i] = x if isinstance(x, int) else x.data_ptr()
         return a
 
-    st = lib.dmuon_step(h, ptrs(params), ptrs(grads), ptrs(momenta), lr, beta, wd, ns_steps,
-                        _stream_handle(stream))
+    if params_ready is None:
+        st = lib.dmuon_step(h, ptrs(params), ptrs(grads), ptrs(momenta), lr, beta, wd, ns_steps,
+                            _stream_handle(stream))
+    else:
+        ev = params_ready if isinstance(params_ready, int) else params_ready.cuda_event
+        st = lib.dmuon_step_ex(h, ptrs(params), ptrs(grads), ptrs(momenta), lr, beta, wd, ns_steps,
+                               _stream_handle(stream), ctypes.c_void_p(ev))
     _lib.check(st, "dmuon_step")
 
 
@@ -189,8 +195,8 @@ class Muon:
                    "dmuon_bind_workspace")
         return self
 
-    def step(self, params, grads, momenta, lr, beta, wd, ns_steps=5, stream=None):
-        dmuon_step(self.handle, params, grads, momenta, lr, beta, wd, ns_steps, stream)
+    def step(self, params, grads, momenta, lr, beta, wd, ns_steps=5, stream=None, params_ready=None):
+        dmuon_step(self.handle, params, grads, momenta, lr, beta, wd, ns_steps, stream, params_ready)
 
     def device_status(self, stream=None) -> int:
         return int(self.lib.dmuon_device_status(self.handle, _stream_handle(stream)))

@@ -56,6 +56,8 @@ SIGNATURES = {
     "dmuon_bind_workspace": (c_int, [c_void_p, c_void_p, c_size_t]),
     "dmuon_step": (c_int, [c_void_p, POINTER(c_void_p), POINTER(c_void_p), POINTER(c_void_p), c_float, c_float,
                            c_float, c_int32, c_void_p]),
+    "dmuon_step_ex": (c_int, [c_void_p, POINTER(c_void_p), POINTER(c_void_p), POINTER(c_void_p), c_float,
+                              c_float, c_float, c_int32, c_void_p, c_void_p]),
     "dmuon_device_status": (c_int, [c_void_p, c_void_p]),
     "dmuon_set_timing": (c_int, [c_void_p, c_int32]),
     "dmuon_get_timing": (c_int, [c_void_p, POINTER(c_double), POINTER(c_int64), c_int32]),

@@ -865,6 +865,11 @@ int dmuon_bind_workspace(dmuon_handle_t h, void* dev_ptr, size_t bytes) {
 
 int dmuon_step(dmuon_handle_t h, void* const* params, const void* const* grads, void* const* momenta, float lr,
                float beta, float wd, int32_t ns_steps, void* stream) {
+    return dmuon_step_ex(h, params, grads, momenta, lr, beta, wd, ns_steps, stream, nullptr);
+}
+
+int dmuon_step_ex(dmuon_handle_t h, void* const* params, const void* const* grads, void* const* momenta, float lr,
+                  float beta, float wd, int32_t ns_steps, void* stream, void* params_ready) {
     if (!h) return fail(DMUON_ERR_INVALID_ARG, "NULL handle");
     if (!h->ws) return fail(DMUON_ERR_NO_WORKSPACE, "no workspace bound (dmuon_bind_workspace)");
     if (!params || !grads || !momenta) return fail(DMUON_ERR_INVALID_ARG, "NULL pointer array");
@@ -906,6 +911,7 @@ int dmuon_step(dmuon_handle_t h, void* const* params, const void* const* grads, 
 
     const auto& per_wave = launches_for(h, ns_steps);
     void* const* dptr = reinterpret_cast<void* const*>(h->ws + h->off_ptrs);
+    bool waited = params_ready == nullptr;
     const float decay = 1.0f - lr * wd;
     for (size_t wi = 0; wi < h->waves.size(); ++wi) {
         const Wave& w = h->waves[wi];
@@ -929,6 +935,14 @@ int dmuon_step(dmuon_handle_t h, void* const* params, const void* const* grads, 
         e = cudaMemsetAsync(h->ws + h->off_counters, 0, per_wave[wi].size() * sizeof(int32_t), s);
         if (e != cudaSuccess) return fail(DMUON_ERR_CUDA, std::string("counter reset: ") + cudaGetErrorString(e));
         for (const Launch& la : per_wave[wi]) {
+            if (!waited && la.timer == DMUON_TIMER_FINAL) {
+                // the first launch that writes parameters: the caller may still
+                // be reading them until params_ready
+                e = cudaStreamWaitEvent(s, static_cast<cudaEvent_t>(params_ready), 0);
+                if (e != cudaSuccess) return fail(DMUON_ERR_CUDA, std::string("wait on params_ready: ") +
+                                                                     cudaGetErrorString(e));
+                waited = true;
+            }
             LaunchList l = la.list;
             l.lr = lr;
             l.decay = decay;

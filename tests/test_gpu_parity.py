@@ -332,3 +332,37 @@ def test_step_replays_from_a_cuda_graph():
     assert e_muon.device_status() == 0 and state[1][0].device_status() == 0
     for a, b in zip(e_ws + e_ms, ws + ms):
         assert torch.equal(a, b)
+
+
+def test_step_ex_waits_for_params_ready_before_the_update():
+    # dmuon_step_ex: the stream waits for params_ready only before the first
+    # parameter write.  An event held back ~50 ms by a spin kernel on another
+    # stream delays the step's end by about that much, and the result equals
+    # dmuon_step's.
+    from matrix_orthogonalising_optimizer_gb300 import Muon
+    shapes = [(320, 704), (300, 300)]
+    inputs = make_inputs(shapes, "bf16", 43)
+    outs = []
+    for use_event in (False, True):
+        muon = Muon([(r, c, 0) for r, c in shapes]).bind()
+        ws = [w.cuda() for w, _, _ in inputs]
+        gs = [g.cuda() for _, g, _ in inputs]
+        ms = [m.cuda().clone() for _, _, m in inputs]
+        muon.step(ws, gs, ms, LR, BETA, WD, 5)  # uploads the pointer table
+        torch.cuda.synchronize()
+        other = torch.cuda.Stream()
+        ready = torch.cuda.Event()
+        with torch.cuda.stream(other):
+            torch.cuda._sleep(100_000_000)  # about 50 ms of spinning
+            ready.record(other)
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record()
+        muon.step(ws, gs, ms, LR, BETA, WD, 5, params_ready=ready if use_event else None)
+        t1.record()
+        torch.cuda.synchronize()
+        assert muon.device_status() == 0
+        outs.append((t0.elapsed_time(t1), [w.cpu() for w in ws]))
+    (t_plain, w_plain), (t_wait, w_wait) = outs
+    assert t_wait > t_plain + 20.0, (t_plain, t_wait)
+    for a, b in zip(w_plain, w_wait):
+        assert torch.equal(a, b)
