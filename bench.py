@@ -165,17 +165,27 @@ def cpu_threads():
     return os.cpu_count()
 
 
-def cpu_baseline(cfg, repeats=1):
-    """Oracle matrices/s for the whole set, extrapolated from one sampled matrix by flop count."""
-    idx = min(range(len(cfg.shapes)), key=lambda i: cfg.shapes[i][0] * cfg.shapes[i][1])
-    r, c = cfg.shapes[idx]
-    t = min(oracle_sample(cfg, idx) for _ in range(repeats))
-    m, n = min(r, c), max(r, c)
+def cpu_baseline(cfg, budget_s=10.0):
+    """Oracle matrices/s for the whole set from a bounded sample: matrices of the set in
+    increasing size, each timed once, until budget_s of oracle time (at least one matrix);
+    the set's time is extrapolated by the oracle's flop count."""
+    order = sorted(range(len(cfg.shapes)), key=lambda i: (cfg.shapes[i][0] * cfg.shapes[i][1], i))
+    t_sum, fl_sum, used = 0.0, 0.0, []
+    for idx in order:
+        if used and t_sum >= budget_s:
+            break
+        r, c = cfg.shapes[idx]
+        t_sum += oracle_sample(cfg, idx)
+        fl_sum += oracle_flops(min(r, c), max(r, c), cfg.ns_steps)
+        used.append(idx)
     total = sum(oracle_flops(min(a, b), max(a, b), cfg.ns_steps) for a, b in cfg.shapes)
-    t_set = t * total / oracle_flops(m, n, cfg.ns_steps)
+    t_set = t_sum * total / fl_sum
+    shapes = sorted({cfg.shapes[i] for i in used})
+    what = ("the whole set" if len(used) == len(cfg.shapes) else
+            f"{len(used)} of {len(cfg.shapes)} matrices, the smallest first ({', '.join(f'{r}x{c}' for r, c in shapes)})")
     return {"value": len(cfg.shapes) / t_set, "unit": "matrices/s", "cores": cpu_threads(), "kind": "oracle",
-            "sample": f"one {r}x{c} matrix (index {idx}) of the set, fp64 direct Newton-Schulz, {t:.2f} s; "
-                      f"set time extrapolated by the oracle's flop count ({t_set:.1f} s per step)"}
+            "sample": f"{what}, fp64 direct Newton-Schulz, {t_sum:.1f} s; set time extrapolated by the "
+                      f"oracle's flop count ({t_set:.1f} s per step)"}
 
 
 # ---------------------------------------------------------------- distributed
@@ -224,9 +234,11 @@ def run_reference(args, cfg, world, rank):
     """The fp64 CPU oracle as the reference arm (rank 0 only)."""
     if rank != 0:
         return
+    # each step a bounded sample, so the whole run stays within a few minutes
+    budget = min(10.0, max(1.0, 120.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
-        cpu_baseline(cfg)
-    vals = [cpu_baseline(cfg) for _ in range(args.steps)]
+        cpu_baseline(cfg, budget)
+    vals = [cpu_baseline(cfg, budget) for _ in range(args.steps)]
     v = statistics.median(x["value"] for x in vals)
     base = dict(vals[0])
     base["value"] = v
