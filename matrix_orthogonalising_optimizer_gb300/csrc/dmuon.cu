@@ -75,7 +75,7 @@ void bucket_buffers(Bucket& b, int32_t precision) {
             set(BUF_BB, m * ldm, ELEM_F32);
         }
     }
-    b.buf_bytes[BUF_PART] = static_cast<int64_t>(up(4 * ((m + 63) / 64) * ((n + 63) / 64), 256));
+    b.buf_bytes[BUF_PART] = static_cast<int64_t>(up(4 * kMomPartials * ((m + 63) / 64) * ((n + 63) / 64), 256));
     b.buf_type[BUF_PART] = ELEM_F32;
     b.pmb = 0;
     for (int k = 0; k < BUF_COUNT; ++k) b.pmb += b.buf_bytes[k];

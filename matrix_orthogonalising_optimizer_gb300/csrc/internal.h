@@ -26,6 +26,7 @@ constexpr int kSimtThreads = 256;
 // momentum / pack tile over the original (rows x cols) matrix
 constexpr int kMomTile = 64;
 constexpr int kMomThreads = 256;
+constexpr int kMomPartials = kMomThreads / 32;  // sum-of-squares partials per momentum tile (one per warp)
 
 constexpr int kMaxGroupsPerLaunch = 96;
 constexpr int kMaxLaunchesPerWave = 1024;  // tile counters in the workspace, cleared per wave
@@ -42,7 +43,7 @@ enum DevStatus : int32_t { DEV_OK = 0, DEV_TIMEOUT = 1 };
 // Per matrix of the plan, in bucket order ("slot").
 struct MatInfo {
     void* x;            // packed u: m x ldx, row-major, transposed for tall matrices
-    float* partials;    // sum-of-squares partials, one per momentum tile
+    float* partials;    // sum-of-squares partials, kMomPartials per momentum tile
     int64_t ldx;        // elements
     int64_t tile_begin; // first momentum tile of this slot inside its wave
     int64_t gidx;       // index of the matrix in the caller's arrays

@@ -6,12 +6,17 @@
 //   u  = grad + beta*M'         (Nesterov; u = M' when disabled)
 // u is written, in the operand dtype, into the bucket's packed [batch, m, n]
 // buffer -- transposed for tall matrices so every packed matrix has m <= n --
-// and sum(u^2) is reduced per 64 x 64 tile.  The finalise kernel sums a
-// matrix's tile partials in a fixed order (so the result does not depend on
+// and sum(u^2) is reduced per warp of each 64 x 64 tile.  The finalise kernel
+// sums a matrix's partials in a fixed order (so the result does not depend on
 // which other matrices share the launch) and writes inv = 1/(||u||_F + eps).
 //
-// HBM-bound: 128-bit loads and stores along rows, the transpose staged
-// through shared memory so both sides stay coalesced.
+// HBM-bound.  Persistent blocks walk the tiles of every matrix of the wave,
+// keeping the current matrix's record and pointers in registers (a lookup
+// per tile would put a chain of dependent loads before every tile's data).
+// Each thread issues its 128-bit grad and momentum loads for both of its rows
+// before using any; stores are 128-bit along rows, the transpose for tall
+// matrices staged through a double-buffered shared tile so both sides stay
+// coalesced with one barrier per transposed tile and none otherwise.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -63,28 +68,73 @@ __device__ __forceinline__ void st1(void* p, int64_t i, int32_t t, float v) {
     else static_cast<float*>(p)[i] = v;
 }
 
-__global__ void __launch_bounds__(kMomThreads) momentum_pack_kernel(const __grid_constant__ MomentumArgs a) {
-    __shared__ float tile[T][T + 1];
-    __shared__ float red[kMomThreads / 32];
-    const int tid = threadIdx.x;
+__device__ __forceinline__ void unpack8(const uint4& q, float (&v)[8]) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&q);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float2 f = __bfloat1622float2(h[k]);
+        v[2 * k] = f.x;
+        v[2 * k + 1] = f.y;
+    }
+}
 
+// Registers are capped so five blocks fit on an SM with both rows' loads in
+// flight per thread.
+constexpr int kMomMinBlocks = 5;
+
+__global__ void __launch_bounds__(kMomThreads, kMomMinBlocks) momentum_pack_kernel(
+    const __grid_constant__ MomentumArgs a) {
+    // two transpose tiles: a block writes one while others may still read the
+    // other, so one barrier per transposed tile is enough
+    __shared__ float tile[2][T][T + 1];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    // the record of the matrix holding this block's current tile, and its
+    // grad and momentum pointers, kept while the block's tiles stay inside it
+    int slot = -1;
+    int64_t begin = 0, end = 0;
+    const void* grad = nullptr;
+    void* mom = nullptr;
+    int buf = 0;
     for (int64_t t = blockIdx.x; t < a.total_tiles; t += gridDim.x) {
-        int lo = 0, hi = a.nslots - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (a.infos[mid].tile_begin <= t) lo = mid;
-            else hi = mid - 1;
+        if (t >= end) {
+            // tiles are numbered matrix after matrix: search forward, trying
+            // the next matrix first
+            int lo = slot + 1, hi = a.nslots - 1;
+            if (lo < hi && a.infos[lo + 1].tile_begin > t) hi = lo;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (a.infos[mid].tile_begin <= t) lo = mid;
+                else hi = mid - 1;
+            }
+            slot = lo;
+            const MatInfo& nm = a.infos[slot];
+            begin = nm.tile_begin;
+            end = begin + nm.ntiles;
+            grad = a.grads[nm.gidx];
+            mom = a.moms[nm.gidx];
         }
-        const MatInfo& mi = a.infos[lo];
-        const int local = static_cast<int>(t - mi.tile_begin);
+        const MatInfo& mi = a.infos[slot];
+        const int local = static_cast<int>(t - begin);
         const int r0 = (local / mi.tiles_c) * T, c0 = (local % mi.tiles_c) * T;
-        const void* grad = a.grads[mi.gidx];
-        void* mom = a.moms[mi.gidx];
         const int rows = mi.rows, cols = mi.cols;
         const int dt = mi.dtype;
         // 128-bit access along rows needs every row start on 16 bytes
         const bool rows_vec = (static_cast<int64_t>(cols) * (dt == ELEM_BF16 ? 2 : 4)) % 16 == 0;
         float ss = 0.0f;
+
+        // bf16 storage: both rows' grad and momentum loads go out before any use
+        const bool bf_vec = dt == ELEM_BF16 && rows_vec;
+        uint4 rg[2], rm[2];
+#pragma unroll
+        for (int p = 0; p < 2; ++p) {
+            const int r = r0 + tid / 8 + 32 * p, c = c0 + (tid % 8) * 8;
+            if (bf_vec && r < rows && c + 8 <= cols) {
+                const int64_t i = static_cast<int64_t>(r) * cols + c;
+                rg[p] = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(grad) + i);
+                rm[p] = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(mom) + i);
+            }
+        }
 
 #pragma unroll
         for (int p = 0; p < 2; ++p) {
@@ -94,8 +144,13 @@ __global__ void __launch_bounds__(kMomThreads) momentum_pack_kernel(const __grid
             if (r < rows && rows_vec && c + 8 <= cols) {
                 const int64_t i = static_cast<int64_t>(r) * cols + c;
                 float g[8], m[8];
-                load8(grad, i, dt, g);
-                load8(mom, i, dt, m);
+                if (bf_vec) {
+                    unpack8(rg[p], g);
+                    unpack8(rm[p], m);
+                } else {
+                    load8(grad, i, dt, g);
+                    load8(mom, i, dt, m);
+                }
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     m[k] = fmaf(a.beta, m[k], g[k]);
@@ -129,11 +184,11 @@ __global__ void __launch_bounds__(kMomThreads) momentum_pack_kernel(const __grid
                 }
             } else {
 #pragma unroll
-                for (int k = 0; k < 8; ++k) tile[rr][cc + k] = u[k];
+                for (int k = 0; k < 8; ++k) tile[buf][rr][cc + k] = u[k];
             }
         }
 
-        if (mi.transposed) {
+        if (mi.transposed) {  // the same for the whole block
             __syncthreads();
             // packed row = original column; 16 consecutive original rows per thread
             const int xr = tid / 4, rr0 = (tid % 4) * 16;
@@ -141,7 +196,7 @@ __global__ void __launch_bounds__(kMomThreads) momentum_pack_kernel(const __grid
             if (c < cols) {
                 float v[16];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) v[e] = tile[rr0 + e][xr];
+                for (int e = 0; e < 16; ++e) v[e] = tile[buf][rr0 + e][xr];
                 const int r = r0 + rr0;
                 const int64_t base = static_cast<int64_t>(c) * mi.ldx + r;
                 if (r + 16 <= rows) {
@@ -159,28 +214,33 @@ __global__ void __launch_bounds__(kMomThreads) momentum_pack_kernel(const __grid
                         if (r + e < rows) st1(mi.x, base + e, mi.x_type, v[e]);
                 }
             }
+            buf ^= 1;
         }
 
-        // deterministic block reduction of sum(u^2)
+        // sum(u^2) of this warp's part of the tile; the finalise adds the
+        // partials in a fixed order
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) ss += __shfl_down_sync(0xffffffffu, ss, o);
-        if ((tid & 31) == 0) red[tid >> 5] = ss;
-        __syncthreads();
-        if (tid == 0) {
-            float s = 0.0f;
-#pragma unroll
-            for (int w = 0; w < kMomThreads / 32; ++w) s += red[w];
-            mi.partials[local] = s;
-        }
-        __syncthreads();
+        if (lane == 0) mi.partials[static_cast<int64_t>(local) * kMomPartials + warp] = ss;
     }
 }
 
-__global__ void __launch_bounds__(256) norm_finalize_kernel(const __grid_constant__ MomentumArgs a) {
-    __shared__ double red[8];
+constexpr int kFinThreads = 256;
+
+__global__ void __launch_bounds__(kFinThreads) norm_finalize_kernel(const __grid_constant__ MomentumArgs a) {
+    __shared__ double red[kFinThreads / 32];
     const MatInfo& mi = a.infos[blockIdx.x];
     double s = 0.0;
-    for (int i = threadIdx.x; i < mi.ntiles; i += 256) s += static_cast<double>(mi.partials[i]);
+    // A tile's partials are two 16-byte loads (the buffer starts on 256 bytes
+    // and a tile's partials take 32).  They are added in fp32 in warp order,
+    // then the tile sums in double: fp64 is slow on this part, so one
+    // conversion and one add per tile.
+    static_assert(kMomPartials == 8, "a tile's partials are read as two float4");
+    const float4* p4 = reinterpret_cast<const float4*>(mi.partials);
+    for (int i = threadIdx.x; i < mi.ntiles; i += kFinThreads) {
+        const float4 x = p4[2 * i], y = p4[2 * i + 1];
+        s += static_cast<double>(x.x + x.y + x.z + x.w + y.x + y.y + y.z + y.w);
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) s += __shfl_down_sync(0xffffffffu, s, o);
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = s;
@@ -188,7 +248,7 @@ __global__ void __launch_bounds__(256) norm_finalize_kernel(const __grid_constan
     if (threadIdx.x == 0) {
         double tot = 0.0;
 #pragma unroll
-        for (int w = 0; w < 8; ++w) tot += red[w];
+        for (int w = 0; w < kFinThreads / 32; ++w) tot += red[w];
         const double inv = 1.0 / (sqrt(tot) + static_cast<double>(a.eps));
         SlotScalars sc;
         sc.inv = static_cast<float>(inv);
@@ -222,7 +282,7 @@ cudaError_t launch_momentum_pack(const MomentumArgs& a, cudaStream_t s) {
 
 cudaError_t launch_norm_finalize(const MomentumArgs& a, cudaStream_t s) {
     if (a.nslots <= 0) return cudaSuccess;
-    norm_finalize_kernel<<<a.nslots, 256, 0, s>>>(a);
+    norm_finalize_kernel<<<a.nslots, kFinThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
 

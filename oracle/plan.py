@@ -53,7 +53,7 @@ def per_matrix_bytes(m: int, n: int, precision: int, route: int, engine: int) ->
             bufs += [m * ldn * 2, m * ldm * 4, m * ldm * 2, m * ldm * 2]  # X1; Af, Ab, B
         else:
             bufs += [m * ldn * 4, m * ldm * 4, m * ldm * 4]              # X1; A, B
-    bufs += [4 * ((m + 63) // 64) * ((n + 63) // 64)]      # sum-of-squares partials
+    bufs += [4 * 8 * ((m + 63) // 64) * ((n + 63) // 64)]  # sum-of-squares partials: 8 per 64 x 64 tile
     return sum(_up(b, 256) for b in bufs)
 
 
