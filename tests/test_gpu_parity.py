@@ -127,6 +127,24 @@ def test_momentum_and_update_ulps():
             assert (d <= (1 if dtype == "bf16" else 4)).mean() >= 0.99, (shapes[i], dtype)
 
 
+def test_momentum_many_one_tile_matrices():
+    # About 1 800 one-tile matrices (half of them tall, so transposed) around a
+    # few larger ragged ones: each block of the momentum kernel then jumps over
+    # hundreds of matrices from one of its tiles to the next.
+    shapes = [(8, 16)] * 900 + [(130, 65)] * 3 + [(16, 8)] * 900 + [(300, 300), (65, 130)]
+    inputs = make_inputs(shapes, "bf16", 21)
+    _, m_new, _ = run_step(shapes, inputs, "bf16", lr=LR, beta=BETA, wd=WD)
+    for i, (w, g, m) in enumerate(inputs):
+        want_m = oracle.round_to_storage(BETA * m.double().numpy() + g.double().numpy(), "bf16")
+        assert ulp_diff(m_new[i], torch.from_numpy(want_m).to(torch.bfloat16)).max() <= 1, (i, shapes[i])
+    # the norms (per-warp partials of every tile) reach O
+    picks = [0, 450, 899, 900, 902, 903, 1500, 1802, 1803, 1804]
+    got, _ = gpu_O(shapes, inputs, "bf16", beta=BETA)
+    want = oracle_O([inputs[i] for i in picks], beta=BETA)
+    errs = [rel_fro(got[i], w) for i, w in zip(picks, want)]
+    assert max(errs) <= TOL["bf16"], max(errs)
+
+
 def test_zero_gradient_gives_pure_decay():
     shapes = [(320, 704), (48, 200), (300, 300)]
     inputs = [(w, torch.zeros_like(g), torch.zeros_like(m)) for w, g, m in make_inputs(shapes, "bf16", 17)]
