@@ -526,6 +526,48 @@ __device__ __forceinline__ void epi_load(const EpiRegs& e, int r, int r0, int la
     else if (r < e.M) load_row(base, type, ld, by_col, r, c0, ncol, x);
 }
 
+// Mirrored half of a 32 x 16 chunk that lies strictly below the diagonal (all
+// its elements stored): element (r0 + lane, c0 + j) also goes to
+// [c0 + j][r0 + lane].  A three-stage exchange inside each group of 8 lanes
+// transposes the chunk in registers (the 8 x 8 blocks of each half of the
+// columns, like quad_transpose one level deeper), so lane (g, t) =
+// (lane / 8, lane % 8) ends with mirrored rows t and 8 + t, columns
+// r0 + 8g .. r0 + 8g + 7, as two 16-byte bf16 pieces: two stores per lane
+// instead of sixteen 2-byte ones.  v is left as it is.  All 32 lanes must call
+// this.
+__device__ __forceinline__ void mirror_words(const float (&v)[CH], int lane, uint4 (&mw)[2]) {
+    float a[CH];
+#pragma unroll
+    for (int j = 0; j < CH; ++j) a[j] = v[j];
+#pragma unroll
+    for (int k = 4; k >= 1; k >>= 1) {
+        const bool hi = (lane & k) != 0;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+            for (int j0 = 0; j0 < 8; ++j0) {
+                if (j0 & k) continue;
+                const int i0 = 8 * h + j0, i1 = 8 * h + (j0 | k);
+                const float send = hi ? a[i0] : a[i1];
+                const float recv = __shfl_xor_sync(kFullMask, send, k);
+                a[i0] = hi ? recv : a[i0];
+                a[i1] = hi ? a[i1] : recv;
+            }
+        }
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+        mw[h] = make_uint4(pack_bf16x2(a[8 * h], a[8 * h + 1]), pack_bf16x2(a[8 * h + 2], a[8 * h + 3]),
+                           pack_bf16x2(a[8 * h + 4], a[8 * h + 5]), pack_bf16x2(a[8 * h + 6], a[8 * h + 7]));
+}
+
+__device__ __forceinline__ void st_mirror(char* base, int64_t ld, int r0, int c0, int lane, const uint4 (&mw)[2]) {
+    __nv_bfloat16* p = reinterpret_cast<__nv_bfloat16*>(base) + r0 + (lane >> 3) * 8;
+    const int t = lane & 7;
+    *reinterpret_cast<uint4*>(p + static_cast<int64_t>(c0 + t) * ld) = mw[0];
+    *reinterpret_cast<uint4*>(p + static_cast<int64_t>(c0 + 8 + t) * ld) = mw[1];
+}
+
 // v (computed in place of the accumulator values) and, for the update, the new
 // W (in place of the loaded W values), to keep the register footprint low.
 __device__ __forceinline__ void epi_finish(const EpiRegs& e, int r, int r0, int lane, int c0, float (&v)[CH],
@@ -553,16 +595,29 @@ __device__ __forceinline__ void epi_finish(const EpiRegs& e, int r, int r0, int 
     if (!upd) {
         // every column of the chunk is stored directly in all 32 rows of the warp
         const bool coop = full && (!e.sym || c0 + CH - 1 < r0);
+        // whole 32-row chunk left of the diagonal block: bf16 mirrors built
+        // once in registers (mirror_words), shared by every mirrored output
+        const bool mfast = coop && e.sym && r0 + 32 <= e.M;
+        uint4 mw[2];
+        bool have_mw = false;
         // last output first, and each output's mirror before its rows: an fp32
         // row store leaves v transposed unless something still needs it
 #pragma unroll
         for (int o = 2; o >= 0; --o) {
             if (!e.out[o]) continue;
-            if (valid && e.out_mirror[o]) {
+            if (e.out_mirror[o]) {
+                if (mfast && e.out_type[o] == ELEM_BF16 && (e.out_ld[o] & 7) == 0) {  // warp-uniform
+                    if (!have_mw) {
+                        mirror_words(v, lane, mw);
+                        have_mw = true;
+                    }
+                    st_mirror(e.out[o], e.out_ld[o], r0, c0, lane, mw);
+                } else if (valid) {
 #pragma unroll
-                for (int j = 0; j < CH; ++j)
-                    if (j < ncol && r > c0 + j)
-                        store_elem(e.out[o], static_cast<int64_t>(c0 + j) * e.out_ld[o] + r, e.out_type[o], v[j]);
+                    for (int j = 0; j < CH; ++j)
+                        if (j < ncol && r > c0 + j)
+                            store_elem(e.out[o], static_cast<int64_t>(c0 + j) * e.out_ld[o] + r, e.out_type[o], v[j]);
+                }
             }
             if (coop) {
                 st_rows(e.out[o], e.out_type[o], e.out_ld[o], r0, c0, lane, v, e.M, o > 0);
