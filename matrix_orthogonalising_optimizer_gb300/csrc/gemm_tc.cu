@@ -443,9 +443,11 @@ __device__ __forceinline__ void ld_rows(const char* base, int32_t type, int64_t 
 
 // The epilogue works on this thread's row r, columns c0 .. c0+CH-1
 // (tcgen05.ld leaves one row per thread).  Row segments move as 16-byte
-// vectors; the mirrored stores of symmetric results, the symmetric aux reads
-// and the transposed W update use the other orientation, where the warp's 32
-// lanes cover 32 consecutive rows and each access is coalesced.
+// vectors, and so do the mirrored halves of symmetric results once transposed
+// in registers (mirror_words); the mirrors of chunks on the diagonal or at a
+// ragged edge, the symmetric aux reads and the transposed W update use the
+// other orientation, where the warp's 32 lanes cover 32 consecutive rows and
+// each access is coalesced.
 //
 // Inputs of a chunk (aux or W) do not depend on the accumulator, so they are
 // loaded one chunk ahead: the first chunk's before the wait for the MMAs, the
