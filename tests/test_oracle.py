@@ -14,6 +14,8 @@ does not reuse the oracle's own arithmetic:
   rational arithmetic by tests/golden/make_quintic_map.py) on diagonal and
   rotated inputs;
 * zero, rank-1, scaled and transposed inputs;
+* the whole update (1 - lr wd) W - lr s O on an input of equal singular
+  values, whose O is f^5(0.25) times its direction (golden table);
 * bf16 round-to-nearest-even against hand-made halfway cases and torch;
 * the planner rules against hand-worked bucket lists.
 """
@@ -254,6 +256,43 @@ def test_update_and_scale_rules():
     out2 = oracle.muon_step(w, grad, mom, lr=lr, beta=beta, wd=wd, dtype="fp32", nesterov=False)
     want2 = oracle.ns_direct(oracle.frobenius_normalise(mom_new.T), 5).T
     assert rel(out2["O"], want2) < 1e-14
+
+
+@pytest.mark.parametrize("dtype,scale_rule", [("fp32", "aspect"), ("bf16", "aspect"), ("fp32", "rms")])
+def test_update_term_closed_form(dtype, scale_rule):
+    # The whole update W' = (1 - lr wd) W - lr s O against a closed form, with
+    # W != 0, lr != 1, wd != 0 and beta != 0, so that every term is visible.
+    # The gradient is k V with V (40 x 16, tall) of orthonormal columns: the
+    # step transposes it to X = (1 + beta) k V^T, whose 16 singular values are
+    # all equal, and normalisation makes each one 0.25 (to 2.5e-13 for the
+    # chosen k).  Newton-Schulz then maps V^T to f^5(0.25) V^T, f^5(0.25) read
+    # from the exact-rational golden table, so O = f^5(0.25) V.  The expected
+    # W' below is written from these facts alone; a dropped lr, a flipped
+    # sign, a wrong decay or scale, or a missing transpose moves W' by far
+    # more than one storage ulp.
+    rows, cols = 40, 16
+    rng = np.random.default_rng(31)
+    v, _ = np.linalg.qr(rng.standard_normal((rows, cols)))   # orthonormal columns
+    lr, wd, beta = _f32(0.02), _f32(0.01), _f32(0.9)
+    big = 1e5 / (1.0 + beta)                                   # (1 + beta) k = 1e5
+    grad = big * v
+    w = oracle.round_to_storage(rng.standard_normal((rows, cols)) * 0.02, dtype)
+    out = oracle.muon_step(w, grad, np.zeros_like(grad), lr=lr, beta=beta, wd=wd, dtype="fp32" if dtype == "fp32"
+                           else "bf16", scale_rule=scale_rule)
+    table = dict((s, vals) for s, vals in _quintic_table())
+    f5 = table[0.25][4]
+    s = math.sqrt(rows / cols) if scale_rule == "aspect" else 0.2 * math.sqrt(max(rows, cols))
+    exact = (1.0 - lr * wd) * w - lr * s * f5 * v
+    assert rel(out["O"], f5 * v) < 1e-10
+    want = oracle.round_to_storage(exact, dtype)
+    st = torch.float32 if dtype == "fp32" else torch.bfloat16
+    got_t, want_t = torch.from_numpy(out["W"]).to(st), torch.from_numpy(want).to(st)
+    # both round values that agree to ~1e-11 relative: equal unless within that of a tie
+    bits = torch.int32 if dtype == "fp32" else torch.int16
+    d = (got_t.view(bits).to(torch.int64) - want_t.view(bits).to(torch.int64)).abs()
+    assert int(d.max()) <= 1 and float((d == 0).double().mean()) >= 0.99
+    # the decay term alone and the update term alone are each far above one ulp here
+    assert np.sqrt(np.mean((lr * wd * w) ** 2)) > 1e-6 and np.sqrt(np.mean((lr * s * f5 * v) ** 2)) > 1e-4
 
 
 def test_gram_method_in_step_matches_direct():
