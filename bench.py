@@ -9,8 +9,12 @@ wd 0.01.  The step is the whole hot path: momentum + pack + norms, the Gram
 products, the Newton-Schulz polynomial products and the final product fused
 with the update.  Inputs (42 GB) are resident in HBM and larger than L2.
 
-Prints one JSON line (rank 0).  ``--impl reference`` times the fp64 CPU
-oracle instead, on a bounded sample of the same workload.
+Prints one JSON line (rank 0).  At N = 1 the line also carries ``configs``:
+the other sets (single 256x1024 fp32 matrix, small transformer, 2 000 mixed
+small matrices, large-layer stress) timed the same way after the headline set,
+each beside the oracle on the host cores.  ``--impl reference`` times the fp64
+CPU oracle instead: each step one seeded matrix of one shape bucket, the set's
+rate extrapolated by bucket counts.
 """
 from __future__ import annotations
 
@@ -44,6 +48,9 @@ def parse_args():
     ap.add_argument("--owners", type=int, default=8,
                     help="owner-model leg: ranks D the set is split over (0 = skip)")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--extra-configs", default="c1,c2,c4,c5",
+                    help="after the headline set, time these sets too (N=1 only; '' = none)")
+    ap.add_argument("--extra-steps", type=int, default=10)
     ap.add_argument("--budget-gb", type=float, default=0.0,
                     help="workspace budget per wave in GiB (0 = the configuration's own)")
     return ap.parse_args()
@@ -165,27 +172,54 @@ def cpu_threads():
     return os.cpu_count()
 
 
-def cpu_baseline(cfg, budget_s=10.0):
-    """Oracle matrices/s for the whole set from a bounded sample: matrices of the set in
-    increasing size, each timed once, until budget_s of oracle time (at least one matrix);
-    the set's time is extrapolated by the oracle's flop count."""
-    order = sorted(range(len(cfg.shapes)), key=lambda i: (cfg.shapes[i][0] * cfg.shapes[i][1], i))
-    t_sum, fl_sum, used = 0.0, 0.0, []
-    for idx in order:
-        if used and t_sum >= budget_s:
-            break
-        r, c = cfg.shapes[idx]
-        t_sum += oracle_sample(cfg, idx)
-        fl_sum += oracle_flops(min(r, c), max(r, c), cfg.ns_steps)
-        used.append(idx)
-    total = sum(oracle_flops(min(a, b), max(a, b), cfg.ns_steps) for a, b in cfg.shapes)
-    t_set = t_sum * total / fl_sum
-    shapes = sorted({cfg.shapes[i] for i in used})
-    what = ("the whole set" if len(used) == len(cfg.shapes) else
-            f"{len(used)} of {len(cfg.shapes)} matrices, the smallest first ({', '.join(f'{r}x{c}' for r, c in shapes)})")
+def _buckets(cfg):
+    """Oracle cost classes of a set: (m, n) -> member indices (tall matrices
+    transposed, as the oracle and the planner both do), smallest first."""
+    b = {}
+    for i, (r, c) in enumerate(cfg.shapes):
+        b.setdefault((min(r, c), max(r, c)), []).append(i)
+    return dict(sorted(b.items(), key=lambda kv: (kv[0][0] * kv[0][1], kv[0])))
+
+
+def cpu_baseline(cfg, full_limit_tflop=2.0):
+    """Oracle matrices/s for the whole set on the host's cores.
+
+    Sets whose oracle work is under ``full_limit_tflop`` (c1, c2) are timed in
+    full.  Larger sets time one seeded matrix of every (m, n) bucket (its first
+    member) and extrapolate the set's time by each bucket's count; the result
+    is labelled "extrapolated" and the per-bucket oracle GFLOP/s are listed."""
+    buckets = _buckets(cfg)
+    T = cfg.ns_steps
+    total_flop = sum(oracle_flops(m, n, T) * len(ix) for (m, n), ix in buckets.items())
+    full = total_flop / 1e12 <= full_limit_tflop
+    per_bucket, t_set, t_timed = [], 0.0, 0.0
+    for (m, n), ix in buckets.items():
+        timed = ix if full else ix[:1]
+        t = sum(oracle_sample(cfg, i) for i in timed)
+        t_timed += t
+        t_one = t / len(timed)
+        t_set += t_one * len(ix)
+        per_bucket.append({"m": m, "n": n, "count": len(ix), "timed": len(timed), "s_per_matrix": t_one,
+                           "oracle_gflops": oracle_flops(m, n, T) / t_one / 1e9})
+    what = ("the whole set, every matrix timed" if full else
+            "one seeded matrix per bucket (" + ", ".join(f"{b['m']}x{b['n']}" for b in per_bucket) +
+            "), set time extrapolated by each bucket's count")
     return {"value": len(cfg.shapes) / t_set, "unit": "matrices/s", "cores": cpu_threads(), "kind": "oracle",
-            "sample": f"{what}, fp64 direct Newton-Schulz, {t_sum:.1f} s; set time extrapolated by the "
-                      f"oracle's flop count ({t_set:.1f} s per step)"}
+            "extrapolated": not full, "per_bucket": per_bucket,
+            "sample": f"{what}; fp64 direct Newton-Schulz, {t_timed:.1f} s of oracle time, "
+                      f"{t_set:.1f} s per step of the whole set"}
+
+
+def cpu_baseline_estimate(cfg, rate_gflops, source):
+    """Oracle matrices/s of a set too large to sample in a bench run (one of
+    its matrices takes minutes): its flop count at a measured oracle rate."""
+    T = cfg.ns_steps
+    total_flop = sum(oracle_flops(min(r, c), max(r, c), T) for r, c in cfg.shapes)
+    t_set = total_flop / (rate_gflops * 1e9)
+    return {"value": len(cfg.shapes) / t_set, "unit": "matrices/s", "cores": cpu_threads(), "kind": "oracle",
+            "extrapolated": True, "estimated": True,
+            "sample": f"not timed (one matrix of this set takes minutes): the set's oracle flop count at "
+                      f"{rate_gflops:.0f} GFLOP/s, the oracle rate measured on {source}"}
 
 
 # ---------------------------------------------------------------- distributed
@@ -231,25 +265,57 @@ def replica_value(n_matrices, world, ms_per_step):
 
 
 def run_reference(args, cfg, world, rank):
-    """The fp64 CPU oracle as the reference arm (rank 0 only)."""
+    """The fp64 CPU oracle as the reference arm (rank 0 only).
+
+    Each step times the oracle on one seeded matrix of one (m, n) bucket of the
+    set, the buckets taken in turn (warm-up steps use the smallest), so every
+    step is a bounded sample and ``ms_per_step`` is its real wall time.  The
+    set's matrices/s is extrapolated from the per-bucket times by each
+    bucket's count (buckets no timed step reached: by the oracle's flop rate
+    on the others)."""
     if rank != 0:
         return
-    # each step a bounded sample, so the whole run stays within a few minutes
-    budget = min(10.0, max(1.0, 120.0 / max(1, args.steps + args.warmup)))
+    buckets = list(_buckets(cfg).items())
+    T = cfg.ns_steps
     for _ in range(args.warmup):
-        cpu_baseline(cfg, budget)
-    vals = [cpu_baseline(cfg, budget) for _ in range(args.steps)]
-    v = statistics.median(x["value"] for x in vals)
-    base = dict(vals[0])
-    base["value"] = v
+        oracle_sample(cfg, buckets[0][1][0])
+    times = {}
+    walls = []
+    for k in range(args.steps):
+        (m, n), ix = buckets[k % len(buckets)]
+        t0 = time.perf_counter()
+        dt = oracle_sample(cfg, ix[0])
+        walls.append(time.perf_counter() - t0)
+        times.setdefault((m, n), []).append(dt)
+    rate = (sum(oracle_flops(m, n, T) * len(v) for (m, n), v in times.items()) /
+            sum(sum(v) for v in times.values()))
+    t_set = 0.0
+    for (m, n), ix in buckets:
+        t_one = statistics.median(times[(m, n)]) if (m, n) in times else oracle_flops(m, n, T) / rate
+        t_set += t_one * len(ix)
+    v = len(cfg.shapes) / t_set
+    ms_step = 1000.0 * statistics.mean(walls)
+    sample = (f"each step one seeded matrix of one (m, n) bucket, the {len(buckets)} buckets in turn "
+              f"({', '.join(f'{m}x{n}' for (m, n), _ in buckets)}); set time extrapolated by each bucket's "
+              f"count: {t_set:.1f} s per step of the whole set")
     print(json.dumps({
         "impl": "reference", "metric": "Muon optimizer-step matrices/s", "value": v, "unit": "matrices/s",
-        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * len(cfg.shapes) / v,
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": workloads_name(cfg), "matrices": len(cfg.shapes), "ns_steps": cfg.ns_steps},
-        "cpu_baseline": base,
+        "config": config_dict(cfg, "auto", 1),
+        "cpu_baseline": {"value": v, "unit": "matrices/s", "cores": cpu_threads(), "kind": "oracle",
+                         "extrapolated": True, "sample": sample},
+        "set_seconds_extrapolated": t_set,
         "e2e": {"value": v, "unit": "matrices/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
+
+
+def config_dict(cfg, routes, world):
+    import workloads
+    return {"workload": workloads_name(cfg), "matrices": len(cfg.shapes), "ns_steps": cfg.ns_steps,
+            "elements": workloads.total_elements(cfg), "lr": cfg.lr, "beta": cfg.beta, "wd": cfg.wd,
+            "l2": "inputs larger than L2 (resident in HBM)",
+            "parallelism": "replicas" if world > 1 else "single GPU", "routes": routes}
 
 
 def workloads_name(cfg):
@@ -334,16 +400,30 @@ def run_dmuon(args, cfg, world, rank, local):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(cfg)
 
+    configs = None
+    if world == 1 and args.extra_configs:
+        import gc
+        del ws, gs, ms, muon
+        gc.collect()
+        torch.cuda.empty_cache()
+        configs = {}
+        rate = None
+        if cpu and cpu.get("per_bucket"):
+            big = max(cpu["per_bucket"], key=lambda b: b["m"] * b["n"])
+            rate = (big["oracle_gflops"], f"the {big['m']}x{big['n']} bucket of {args.config}")
+        for name in [c for c in args.extra_configs.split(",") if c and c != args.config]:
+            est = rate if name == "c5" else None
+            configs[name] = measure_config(name, args.extra_steps if name != "c5" else 3, 3 if name != "c5" else 2,
+                                           peaks, src, cpu=not args.no_cpu_baseline and (name != "c5" or rate),
+                                           oracle_rate=est)
+
     if rank == 0:
         line = {
             "metric": "Muon optimizer-step matrices/s", "value": value, "unit": "matrices/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if cfg.precision == "bf16" else "fp32",
             "data": "synthetic",
-            "config": {"workload": workloads_name(cfg), "matrices": n_mat, "ns_steps": T,
-                       "elements": workloads.total_elements(cfg), "lr": lr, "beta": beta, "wd": wd,
-                       "l2": "inputs larger than L2 (resident in HBM)",
-                       "parallelism": "replicas" if world > 1 else "single GPU", "routes": args.routes},
+            "config": config_dict(cfg, args.routes, world),
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak,
                          "traffic": measured_traffic() if args.config == "c3" else None,
@@ -354,11 +434,93 @@ def run_dmuon(args, cfg, world, rank, local):
             "step_frac_of_peak": flops_total / (ms_step / 1000.0) / 1e12 / peak,
             "stages_ms_per_step": stages, "launches_per_step": launches_per_step,
             "gpu_launches": int(launches), "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu,
-            "adamw": adamw, "owner_model": owners,
+            "adamw": adamw, "owner_model": owners, "configs": configs,
             "muon_over_adamw_step_time": ms_step / adamw["ms_per_step"] if adamw and "ms_per_step" in adamw
             else None,
         }
         print(json.dumps(line), flush=True)
+
+
+L2_BYTES = 129 * 10 ** 6
+
+
+def measure_config(name, steps, warmup, peaks, src, cpu, oracle_rate=None):
+    """One more workload, timed like the headline one: ms/step, matrices/s, the
+    tcgen05 GEMM fraction of peak and the stage split, and beside it the oracle
+    on the host (``cpu``).  Sets whose inputs fit in L2 have L2 flushed
+    (a 512 MB write) before every timed step, each step timed alone."""
+    import gc
+
+    import torch
+
+    import workloads
+    from matrix_orthogonalising_optimizer_gb300 import Muon
+    cfg = workloads.get(name)
+    dt = 0 if cfg.dtype == "bf16" else 1
+    esz = 2 if cfg.dtype == "bf16" else 4
+    budget = int(cfg.budget_gb * (1 << 30))
+    muon = Muon([(r, c, dt) for r, c in cfg.shapes], precision=cfg.precision, workspace_budget=budget)
+    inputs = 3 * workloads.total_elements(cfg) * esz
+    free, _ = torch.cuda.mem_get_info()
+    if inputs + muon.workspace_bytes() + (4 << 30) > free:
+        return {"workload": workloads_name(cfg),
+                "skipped": f"needs {(inputs + muon.workspace_bytes()) / 1e9:.0f} GB, {free / 1e9:.0f} GB free"}
+    muon.bind()
+    ws, gs, ms = workloads.make_set(cfg, "cuda")
+    lr, beta, wd, T = cfg.lr, cfg.beta, cfg.wd, cfg.ns_steps
+    stream = torch.cuda.current_stream()
+    flush = inputs < 2 * L2_BYTES
+    scrub = torch.empty(512 << 20, dtype=torch.uint8, device="cuda") if flush else None
+    for _ in range(warmup):
+        muon.step(ws, gs, ms, lr, beta, wd, T, stream)
+    torch.cuda.synchronize()
+    muon.set_timing(True)
+    per_step = []
+    if flush:
+        for _ in range(steps):
+            scrub.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            muon.step(ws, gs, ms, lr, beta, wd, T, stream)
+            e1.record(stream)
+            per_step.append((e0, e1))
+        torch.cuda.synchronize()
+        ms_step = sum(a.elapsed_time(b) for a, b in per_step) / steps
+    else:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            muon.step(ws, gs, ms, lr, beta, wd, T, stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms_step = e0.elapsed_time(e1) / steps
+    timing = muon.timing()
+    muon.set_timing(False)
+    status = muon.device_status(stream)
+    flops_total, flops_tc = muon.flops(T)
+    del ws, gs, ms, muon, scrub
+    gc.collect()
+    torch.cuda.empty_cache()
+    if status != 0:
+        raise RuntimeError(f"device status set in the {name} measurement")
+    peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    tc_ms = timing["tc"][0] / steps
+    out = {"workload": workloads_name(cfg), "matrices": len(cfg.shapes), "steps": steps, "warmup": warmup,
+           "ms_per_step": ms_step, "matrices_per_s": len(cfg.shapes) / (ms_step / 1000.0),
+           "dtype": "bf16" if cfg.precision == "bf16" else "fp32",
+           "l2": "L2 flushed (512 MB write) before every timed step" if flush
+           else "inputs larger than L2 (resident in HBM)",
+           "stages_ms_per_step": {k: round(v[0] / steps, 4) for k, v in timing.items()},
+           "launches_per_step": {k: v[1] // steps for k, v in timing.items()},
+           "step_tflops": flops_total / (ms_step / 1000.0) / 1e12}
+    if flops_tc > 0 and tc_ms > 0:
+        achieved = flops_tc / (tc_ms / 1000.0) / 1e12
+        out["gemm"] = {"algorithmic_tflop_per_step": flops_tc / 1e12, "achieved_tflops": achieved,
+                       "frac_of_sustained_peak": achieved / peak, "peak_source": f"bf16_tflops_sustained of {src} peaks"}
+    if cpu:
+        out["cpu_baseline"] = (cpu_baseline(cfg) if oracle_rate is None
+                               else cpu_baseline_estimate(cfg, *oracle_rate))
+    return out
 
 
 def _time_subset(cfg, idx, ws, gs, ms, stream, warmup=2, steps=3):

@@ -133,7 +133,10 @@ typedef struct {
 
 /* ---- planning (host only: no CUDA call, works without a GPU) ---------- */
 
-/* Shape-bucketing planner.  Each shape is canonicalised to (m, n, transposed)
+/* Shape-bucketing planner (DMuon technical summary on gist.science, section
+ * 2.2, "batching": matrices of like shape are grouped so that small ones do
+ * not leave the GPU idle; the Gram iteration takes the short side m < n).
+ * Each shape is canonicalised to (m, n, transposed)
  * with m = min(rows, cols), n = max(rows, cols), transposed = rows > cols
  * (tall matrices are packed transposed), and its route resolved: the shape's
  * own rule, else options->route; AUTO gives Gram when n >= 3m or m <=
@@ -160,7 +163,8 @@ int64_t dmuon_plan_wave_num_pieces(dmuon_handle_t h, int64_t wave);
 /* piece = matrices [start, start+count) of bucket `bucket` (bucket order) */
 int dmuon_plan_wave_piece(dmuon_handle_t h, int64_t wave, int64_t piece,
                           int64_t* bucket, int64_t* start, int64_t* count);
-/* Algorithmic FLOPs of one step with `ns_steps` iterations: 2 per
+/* Algorithmic FLOPs of one step with `ns_steps` iterations (section 2.2,
+ * "symmetry": the symmetric products count half): 2 per
  * multiply-add, symmetric outputs counted once (SYRK and the m x m products
  * at half).  Gram bucket: (3 m^2 n + (4T-3) m^3) per matrix; direct bucket:
  * T (3 m^2 n + m^3).  Written to out[0]; out[1] gets the part run on tensor
@@ -169,7 +173,9 @@ int dmuon_plan_flops(dmuon_handle_t h, int32_t ns_steps, double* out);
 
 /* ---- workspace --------------------------------------------------------- */
 
-/* Device bytes the caller must provide (256-byte aligned). */
+/* Device bytes the caller must provide (256-byte aligned).  No counterpart
+ * in the paper (its module plugs into the training framework and allocates
+ * there, section 2 and the abstract); here the caller owns every device byte. */
 size_t dmuon_workspace_bytes(dmuon_handle_t h);
 /* Binds caller-owned device memory (e.g. a torch uint8 tensor) of at least
  * dmuon_workspace_bytes(h) bytes, 256-byte aligned, on the current device.
@@ -180,7 +186,10 @@ int dmuon_bind_workspace(dmuon_handle_t h, void* dev_ptr, size_t bytes);
 
 /* ---- the step ---------------------------------------------------------- */
 
-/* One Muon step over every planned matrix (formula in the file header).
+/* One Muon step over every planned matrix (formula in the file header):
+ * the per-owner compute of section 2.2 -- Newton-Schulz on the
+ * momentum-aggregated gradient (section 1) carried in the Gram space, then
+ * Muon's update rule, unchanged (section 5).
  * params[i], grads[i], momenta[i]: device pointers of shape i.  lr, wd >= 0,
  * 0 <= beta < 1 (finite), 1 <= ns_steps <= DMUON_MAX_NS_STEPS.  Errors:
  * INVALID_ARG (NULL arrays or pointers, bad scalars), ALIGN,
@@ -189,7 +198,9 @@ int dmuon_step(dmuon_handle_t h, void* const* params, const void* const* grads,
                void* const* momenta, float lr, float beta, float wd,
                int32_t ns_steps, void* stream);
 
-/* dmuon_step, with one more ordering point: if params_ready (a cudaEvent_t
+/* No counterpart in the paper (overlap of the caller's parameter copies with
+ * the step, in the spirit of section 2.2's overlap of communication and
+ * compute).  dmuon_step, with one more ordering point: if params_ready (a cudaEvent_t
  * passed as void*) is not NULL, `stream` waits for it right before the first
  * launch that writes the parameters -- the final product of the first wave;
  * the momentum, normalisation and Newton-Schulz launches before it do not
@@ -200,7 +211,8 @@ int dmuon_step(dmuon_handle_t h, void* const* params, const void* const* grads,
 int dmuon_step_ex(dmuon_handle_t h, void* const* params, const void* const* grads, void* const* momenta,
                   float lr, float beta, float wd, int32_t ns_steps, void* stream, void* params_ready);
 
-/* Synchronises `stream`, returns the device status word (DMUON_OK or
+/* No counterpart in the paper (bounded device waits are this library's).
+ * Synchronises `stream`, returns the device status word (DMUON_OK or
  * DMUON_ERR_DEVICE_TIMEOUT) and clears it. */
 int dmuon_device_status(dmuon_handle_t h, void* stream);
 
@@ -215,7 +227,9 @@ int dmuon_device_status(dmuon_handle_t h, void* stream);
 #define DMUON_TIMER_SIMT 6     /* every fp32 FFMA GEMM launch (sum) */
 #define DMUON_TIMER_COUNT 7
 
-/* enable != 0 records a CUDA event pair around every launch of later steps
+/* Stage timers (the paper reports optimizer-step time per stage of its
+ * pipeline, section 4; no API of its own).
+ * enable != 0 records a CUDA event pair around every launch of later steps
  * (on the step's stream).  Resets the accumulated times. */
 int dmuon_set_timing(dmuon_handle_t h, int32_t enable);
 /* Synchronises the recorded events and writes, per DMUON_TIMER_* slot, the
@@ -238,7 +252,8 @@ const char* dmuon_status_string(int status);
                                  (bf16 on tensor cores, the fp32 buffer otherwise): both
                                  triangles, bitwise symmetric */
 
-/* Byte offset into the bound workspace, leading dimension (elements), batch
+/* No counterpart in the paper (test inspection of the symmetric operands of
+ * section 2.2).  Byte offset into the bound workspace, leading dimension (elements), batch
  * stride (elements) and element dtype (DMUON_BF16 | DMUON_FP32; may be NULL)
  * of buffer `which` of piece (wave, piece). */
 int dmuon_debug_buffer(dmuon_handle_t h, int64_t wave, int64_t piece, int32_t which,
@@ -327,8 +342,10 @@ int dmuon_adamw_status(void);
  * min(rows, cols) <= 128 and rows*cols <= 262144; larger shapes return
  * DMUON_ERR_INVALID_ARG with the limit in dmuon_last_error().  It calls no
  * cudaMalloc, cudaFree or other allocating routine.  The first call on a
- * device looks up the array's device address (cudaGetSymbolAddress, with
- * that device current); make that first call before any stream capture.
+ * device (and the first after its context was destroyed and re-created, e.g.
+ * by cudaDeviceReset) looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current) and caches it with the
+ * context's unique id; make that first call before any stream capture.
  * All calls on a device share the array: calls that may overlap on the GPU
  * (unordered streams) race on it and must be serialised by the caller.
  * Returns DMUON_OK, DMUON_ERR_INVALID_ARG, DMUON_ERR_ALIGN,

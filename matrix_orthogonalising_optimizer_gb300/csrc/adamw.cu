@@ -346,14 +346,13 @@ extern "C" int dmuon_adamw_step(void* const* params, const void* const* grads, v
                                                   cudaSuccess)
         return fail(DMUON_ERR_CUDA, "dmuon_adamw_step: no CUDA device");
     const size_t smem = sizeof(AdamSmem) + 128;
-    static int configured_device = -1;
-    if (configured_device != dev) {
-        const cudaError_t e =
-            cudaFuncSetAttribute(adamw_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-        if (e != cudaSuccess)
-            return fail(DMUON_ERR_CUDA, std::string("dmuon_adamw_step: ") + cudaGetErrorString(e));
-        configured_device = dev;
-    }
+    // the shared-memory attribute, once per device with that device current
+    static dmuon::PerDevice configured;
+    int unused = 0;
+    const cudaError_t ce = configured.get(dev, &unused, [&](int*) {
+        return cudaFuncSetAttribute(adamw_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    });
+    if (ce != cudaSuccess) return fail(DMUON_ERR_CUDA, std::string("dmuon_adamw_step: ") + cudaGetErrorString(ce));
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     int64_t i = 0;
     while (i < count) {

@@ -999,7 +999,7 @@ size_t gemm_tc_smem_bytes() { return sizeof(Smem) + 1024; }
 
 cudaError_t launch_gemm_tc(const LaunchList& l, int num_sms, cudaStream_t s) {
     if (l.total_tiles <= 0) return cudaSuccess;
-    static int max_pairs = 0;
+    static PerDevice max_pairs_per_device;
     const size_t smem = gemm_tc_smem_bytes();
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -1012,16 +1012,25 @@ cudaError_t launch_gemm_tc(const LaunchList& l, int num_sms, cudaStream_t s) {
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (max_pairs == 0) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    // the shared-memory attribute is set, and the resident pairs counted, once
+    // per device with that device current
+    int max_pairs = 0;
+    e = max_pairs_per_device.get(dev, &max_pairs, [&](int* out) {
+        cudaError_t r = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-        cfg.gridDim = dim3(num_sms / kPair * kPair);
+        if (r != cudaSuccess) return r;
+        cudaLaunchConfig_t probe = cfg;
+        probe.gridDim = dim3(num_sms / kPair * kPair);
         int n = 0;
-        e = cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel, &cfg);
-        if (e != cudaSuccess) return e;
-        max_pairs = n > 0 ? n : num_sms / kPair;
-    }
+        r = cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel, &probe);
+        if (r != cudaSuccess) return r;
+        *out = n > 0 ? n : num_sms / kPair;
+        return cudaSuccess;
+    });
+    if (e != cudaSuccess) return e;
     const int pairs = l.total_tiles < max_pairs ? l.total_tiles : max_pairs;
     cfg.gridDim = dim3(pairs * kPair);
     return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, l);

@@ -5,6 +5,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cstdint>
+#include <mutex>
 
 namespace dmuon {
 
@@ -120,6 +121,37 @@ struct MomentumArgs {
     float beta;
     int32_t nesterov;
     float eps;
+};
+
+// ---------------------------------------------------------------- per device
+
+constexpr int kMaxCachedDevices = 64;
+
+// A launch setting computed once per device with that device current (an
+// occupancy figure, or a kernel attribute that must be set before the first
+// launch on each device).  Thread-safe; devices beyond kMaxCachedDevices are
+// computed on every call.
+class PerDevice {
+  public:
+    template <typename F>
+    cudaError_t get(int dev, int* out, F&& compute) {
+        if (dev < 0 || dev >= kMaxCachedDevices) return compute(out);
+        std::lock_guard<std::mutex> lock(mu_);
+        if (!done_[dev]) {
+            int v = 0;
+            const cudaError_t e = compute(&v);
+            if (e != cudaSuccess) return e;
+            val_[dev] = v;
+            done_[dev] = true;
+        }
+        *out = val_[dev];
+        return cudaSuccess;
+    }
+
+  private:
+    std::mutex mu_;
+    int val_[kMaxCachedDevices] = {};
+    bool done_[kMaxCachedDevices] = {};
 };
 
 // ---------------------------------------------------------------- launchers

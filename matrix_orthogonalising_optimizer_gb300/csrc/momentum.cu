@@ -266,14 +266,16 @@ cudaError_t launch_momentum_pack(const MomentumArgs& a, cudaStream_t s) {
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     // persistent blocks: exactly as many as fit at once (a grid of 8 per SM,
     // 6 resident, ran its last 2 per SM as a second wave after the others)
-    static int per_sm = 0;
-    if (per_sm == 0) {
+    static PerDevice per_sm_per_device;
+    int per_sm = 1;
+    per_sm_per_device.get(dev, &per_sm, [](int* out) {
         int n = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, momentum_pack_kernel, kMomThreads, 0) != cudaSuccess ||
             n < 1)
             n = 1;
-        per_sm = n;
-    }
+        *out = n;
+        return cudaSuccess;
+    });
     const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 1) * per_sm;
     const int grid = static_cast<int>(a.total_tiles < cap ? a.total_tiles : cap);
     momentum_pack_kernel<<<grid, kMomThreads, 0, s>>>(a);

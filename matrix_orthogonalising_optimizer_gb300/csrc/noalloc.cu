@@ -159,8 +159,42 @@ __global__ void __launch_bounds__(kThreads) muon_small_kernel(const __grid_const
     }
 }
 
+// The device address of the scratch is looked up once per CUDA context and
+// cached with the context's unique id: after the context is destroyed (for
+// example by cudaDeviceReset) and a new one is created, the module is loaded
+// again and the array may sit elsewhere, so a new id triggers a new lookup.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
 std::mutex g_mu;
-float* g_scratch_ptr[kMaxDevices] = {};
+struct ScratchEntry {
+    unsigned long long ctx_id;
+    float* ptr;
+};
+ScratchEntry g_scratch[kMaxDevices] = {};
+CtxGetCurrentFn g_ctx_current = nullptr;
+CtxGetIdFn g_ctx_id = nullptr;
+
+// Unique id of the calling thread's current context (0 if none is current).
+bool current_context_id(unsigned long long* id) {
+    if (!g_ctx_current || !g_ctx_id) {
+        void* f0 = nullptr;
+        void* f1 = nullptr;
+        cudaDriverEntryPointQueryResult q0, q1;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f0, 4000, cudaEnableDefault, &q0) != cudaSuccess ||
+            q0 != cudaDriverEntryPointSuccess || !f0 ||
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &f1, 12000, cudaEnableDefault, &q1) != cudaSuccess ||
+            q1 != cudaDriverEntryPointSuccess || !f1)
+            return false;
+        g_ctx_current = reinterpret_cast<CtxGetCurrentFn>(f0);
+        g_ctx_id = reinterpret_cast<CtxGetIdFn>(f1);
+    }
+    CUcontext ctx = nullptr;
+    if (g_ctx_current(&ctx) != CUDA_SUCCESS) return false;
+    *id = 0;
+    if (!ctx) return true;
+    return g_ctx_id(ctx, id) == CUDA_SUCCESS;
+}
 
 }  // namespace
 
@@ -180,7 +214,9 @@ extern "C" int dmuon_step_noalloc(void* param, const void* grad, void* momentum,
         set_last_error("dmuon_step_noalloc: unknown dtype");
         return DMUON_ERR_UNSUPPORTED_DTYPE;
     }
-    if (rows < 1 || cols < 1 || (rows < cols ? rows : cols) > kMaxM || rows * cols > kMaxElems) {
+    // each side is bounded before the product, so rows * cols cannot overflow
+    if (rows < 1 || cols < 1 || rows > kMaxElems || cols > kMaxElems || (rows < cols ? rows : cols) > kMaxM ||
+        rows * cols > kMaxElems) {
         set_last_error("dmuon_step_noalloc: " + std::to_string(rows) + "x" + std::to_string(cols) +
                        " exceeds the static scratch: need min(rows, cols) <= 128 and rows*cols <= 262144");
         return DMUON_ERR_INVALID_ARG;
@@ -197,10 +233,16 @@ extern "C" int dmuon_step_noalloc(void* param, const void* grad, void* momentum,
     }
     float* scratch = nullptr;
     {
-        // once per device, with that device current: the device address of
-        // the static scratch (the host-side symbol is not a device address)
+        // once per device and context, with that device current: the device
+        // address of the static scratch (the host-side symbol is not a device
+        // address)
         std::lock_guard<std::mutex> lock(g_mu);
-        if (!g_scratch_ptr[dev]) {
+        unsigned long long id = 0;
+        if (!current_context_id(&id)) {
+            set_last_error("dmuon_step_noalloc: cannot query the current CUDA context");
+            return DMUON_ERR_CUDA;
+        }
+        if (id == 0 || !g_scratch[dev].ptr || g_scratch[dev].ctx_id != id) {
             void* p = nullptr;
             const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
             if (e != cudaSuccess || !p) {
@@ -208,9 +250,15 @@ extern "C" int dmuon_step_noalloc(void* param, const void* grad, void* momentum,
                                cudaGetErrorString(e));
                 return DMUON_ERR_CUDA;
             }
-            g_scratch_ptr[dev] = static_cast<float*>(p);
+            // the lookup makes the device's primary context current if none was
+            if (id == 0 && !current_context_id(&id)) {
+                set_last_error("dmuon_step_noalloc: cannot query the current CUDA context");
+                return DMUON_ERR_CUDA;
+            }
+            g_scratch[dev].ptr = static_cast<float*>(p);
+            g_scratch[dev].ctx_id = id;
         }
-        scratch = g_scratch_ptr[dev];
+        scratch = g_scratch[dev].ptr;
     }
     SmallArgs a;
     a.w = param;

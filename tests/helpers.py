@@ -80,3 +80,39 @@ def oracle_O(inputs, *, beta, ns_steps=5, nesterov=True, coeffs=oracle.NS_COEFFS
                                     beta=beta, wd=0.0, ns_steps=ns_steps, nesterov=nesterov, coeffs=coeffs,
                                     dtype="fp32")["O"])
     return res
+
+
+def check_update_against_oracle(w_gpu, w_in, want, o_orc, *, lr, wd, scale, dtype, tau):
+    """W' from the GPU against the oracle's W' (not against the GPU's own O).
+
+    The two differ by (a) one rounding of each to the storage dtype, (b) the
+    kernel's fp32 arithmetic (decay = fl(1 - lr wd), fl(decay W), fl(lr s):
+    at most 2^-23 |W| + 2^-23 lr s |O|), and (c) lr s (O_gpu - O_oracle), which
+    the O parity bounds in Frobenius norm by lr s tau ||O||_F.  So:
+
+    * Frobenius bar: what is left of |W'_gpu - W'_oracle| after (a) and (b)
+      is at most lr s tau ||O_oracle||_F;
+    * ulp bar on the elements whose storage ulp is at least 4 lr s tau
+      rms(O): there the O tolerance cannot move W' by a whole ulp, so
+      >= 99.9 % are within 1 ulp and all within 2.  (Elements near W' = 0 have
+      a tiny ulp that the allowed O error spans many times: an ulp bar over
+      all elements would test the O error again, not the update.)
+
+    w_gpu, w_in: torch tensors (storage dtype); want, o_orc: float64 arrays.
+    Returns (excess ratio, subset fraction, fraction within 1 ulp in the subset).
+    """
+    got = w_gpu.double().numpy()
+    w64 = w_in.double().numpy()
+    ulp = ulp_of(want, dtype)
+    arith = 2.0 ** -23 * (np.abs(w64) + lr * scale * np.abs(o_orc))
+    excess = np.maximum(np.abs(got - want) - ulp - arith, 0.0)
+    allowed = lr * scale * tau * np.linalg.norm(o_orc)
+    ratio = float(np.linalg.norm(excess) / allowed)
+    assert ratio <= 1.0, f"W' excess {ratio:.3f} of what the O tolerance allows"
+    sub = ulp >= 4.0 * lr * scale * tau * np.sqrt(np.mean(o_orc * o_orc))
+    frac1 = 1.0
+    if sub.sum() >= 1000:
+        d = ulp_diff(w_gpu, torch.from_numpy(want).to(w_gpu.dtype))[sub]
+        frac1 = float((d <= 1).mean())
+        assert frac1 >= 0.999 and d.max() <= 2, (frac1, int(d.max()))
+    return ratio, float(sub.mean()), frac1

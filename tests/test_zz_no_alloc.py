@@ -3,8 +3,8 @@
 Callers that cannot allocate device memory (their GPU memory is held by
 another allocator, or they run under a fixed budget) cannot give dmuon_step
 its workspace; this entry point keeps its scratch in a static device array
-instead.  Here it is called through the C ABI twice in a row, on different
-shapes and dtypes, and compared with dmuon_step in its fp32 validation mode
+instead.  Here it is called through the C ABI three times in a row, on shapes with
+different short sides and on both dtypes, and compared with dmuon_step in its fp32 validation mode
 (the same arithmetic) on the same inputs: the momentum must match exactly and
 the orthogonalised update O within the fp32 tolerance of 1e-4.
 """
@@ -43,11 +43,14 @@ def _workspace_step(w, g, m, dtype, lr, wd):
     muon.step([w], [g], [m], lr, BETA, wd, 5)
 
 
-def test_noalloc_matches_workspace_step_twice_in_a_row():
+def test_noalloc_matches_workspace_step_three_calls_in_a_row():
     if not torch.cuda.is_available():
         pytest.skip("needs a GPU")
     lib = _lib.load(build_if_missing=True)
-    for rows, cols, dtype, seed in [(96, 700, "bf16", 41), (700, 96, "fp32", 42)]:
+    # three calls in a row whose short side changes (128, 40, 96), so each
+    # call's scratch layout differs from the one before; a tall bf16 matrix
+    # takes the transposed load and store path
+    for rows, cols, dtype, seed in [(128, 2048, "bf16", 41), (700, 40, "bf16", 42), (96, 700, "fp32", 43)]:
         w, g, m = _inputs(rows, cols, dtype, seed)
         s = oracle.shape_scale(rows, cols)
         outs = {}
@@ -85,7 +88,8 @@ def test_noalloc_rejects_shapes_beyond_the_scratch():
     lib = _lib.load(build_if_missing=True)
     buf = torch.zeros(1 << 19, dtype=torch.float32, device="cuda")
     p = ctypes.c_void_p(buf.data_ptr())
-    for rows, cols in [(129, 300), (300, 129), (64, 5000)]:
+    # the last two overflow int64 if multiplied before the sides are bounded
+    for rows, cols in [(129, 300), (300, 129), (64, 5000), (128, 1 << 57), (1 << 40, 1 << 40)]:
         st = lib.dmuon_step_noalloc(p, p, p, rows, cols, 1, LR, BETA, WD, 5, None)
         assert st == _lib.ERR_INVALID_ARG
         assert b"262144" in lib.dmuon_last_error()
