@@ -92,11 +92,14 @@ def check_update_against_oracle(w_gpu, w_in, want, o_orc, *, lr, wd, scale, dtyp
 
     * Frobenius bar: what is left of |W'_gpu - W'_oracle| after (a) and (b)
       is at most lr s tau ||O_oracle||_F;
-    * ulp bar on the elements whose storage ulp is at least 4 lr s tau
-      rms(O): there the O tolerance cannot move W' by a whole ulp, so
-      >= 99.9 % are within 1 ulp and all within 2.  (Elements near W' = 0 have
-      a tiny ulp that the allowed O error spans many times: an ulp bar over
-      all elements would test the O error again, not the update.)
+    * ulp bar where the O tolerance cannot move W' by a whole ulp: on the
+      elements whose storage ulp is at least 4 lr s tau max(|O_ij|, rms(O)),
+      >= 99.9 % are within 1 ulp and all within 2.  An element's share of the
+      O error grows with its own |O_ij|: with heavy-tailed gradients (1 % of
+      entries x100) a few outputs are 25x the rms and carry errors of a few
+      percent of themselves, i.e. several ulps of W'.  Elements near W' = 0
+      have a tiny ulp that the allowed O error spans many times.  An ulp bar
+      over all elements would test the O error again, not the update.
 
     w_gpu, w_in: torch tensors (storage dtype); want, o_orc: float64 arrays.
     Returns (excess ratio, subset fraction, fraction within 1 ulp in the subset).
@@ -109,10 +112,13 @@ def check_update_against_oracle(w_gpu, w_in, want, o_orc, *, lr, wd, scale, dtyp
     allowed = lr * scale * tau * np.linalg.norm(o_orc)
     ratio = float(np.linalg.norm(excess) / allowed)
     assert ratio <= 1.0, f"W' excess {ratio:.3f} of what the O tolerance allows"
-    sub = ulp >= 4.0 * lr * scale * tau * np.sqrt(np.mean(o_orc * o_orc))
-    frac1 = 1.0
+    rms = np.sqrt(np.mean(o_orc * o_orc))
+    sub = ulp >= 4.0 * lr * scale * tau * np.maximum(np.abs(o_orc), rms)
+    frac1, worst = 1.0, 0
     if sub.sum() >= 1000:
         d = ulp_diff(w_gpu, torch.from_numpy(want).to(w_gpu.dtype))[sub]
-        frac1 = float((d <= 1).mean())
-        assert frac1 >= 0.999 and d.max() <= 2, (frac1, int(d.max()))
+        frac1, worst = float((d <= 1).mean()), int(d.max())
+        assert frac1 >= 0.999 and worst <= 2, (frac1, worst)
+    print(f"W' vs oracle {tuple(w_gpu.shape)} {dtype}: excess {ratio:.3f} of allowed; ulp-bar subset "
+          f"{sub.mean():.3f}, within 1 ulp there {frac1:.5f}, worst {worst}")
     return ratio, float(sub.mean()), frac1

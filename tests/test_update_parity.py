@@ -7,8 +7,8 @@ wd = 0.01, and W' is compared with the oracle's own rounded W'
 tolerance (tests/helpers.check_update_against_oracle): after one storage
 rounding and the kernel's fp32 arithmetic, what is left of W'_gpu - W'_oracle
 is at most lr*s*tau*||O||_F in Frobenius norm, and where the storage ulp is
-large against lr*s*tau*rms(O), >= 99.9 % of W' are within 1 ulp and all
-within 2.  M' is checked within 1 ulp of the oracle's.
+large against lr*s*tau*max(|O_ij|, rms(O)), >= 99.9 % of W' are within 1 ulp
+and all within 2.  M' is checked within 1 ulp of the oracle's.
 """
 import numpy as np
 import pytest
