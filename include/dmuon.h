@@ -75,6 +75,10 @@ extern "C" {
 #define DMUON_BUCKET_DIRECT 2
 #define DMUON_ENGINE_TC_BF16 0 /* tensor cores, bf16 operands */
 #define DMUON_ENGINE_SIMT_FP32 1 /* fp32 FFMA */
+#define DMUON_ENGINE_TC_SPLIT 2 /* tensor cores, split-bf16 operands: each m x m operand
+                                   x = hi + lo (hi = bf16(x), lo = bf16(x - hi)) and each
+                                   product hi*hi + hi*lo + lo*hi; the final product's Q
+                                   as hi + lo */
 
 /* update-scale rules */
 #define DMUON_SCALE_ASPECT 0 /* s = sqrt(max(1, rows/cols)) */
@@ -116,7 +120,8 @@ typedef struct {
     int32_t scale_rule;     /* DMUON_SCALE_*; default ASPECT */
     int32_t no_nesterov;    /* 0 => Nesterov U = grad + beta*M'; 1 => U = M' */
     int32_t small_m;        /* AUTO route and BF16 mode: Gram buckets with m <= small_m run
-                               their m x m products in fp32 FFMA; 0 => 256; < 0 => none */
+                               their m x m products on split-bf16 tensor cores
+                               (DMUON_ENGINE_TC_SPLIT); 0 => 256; < 0 => none */
     int32_t reserved;
     uint64_t workspace_budget; /* bytes for one wave of buckets; 0 => everything in one wave */
 } dmuon_options_t;
@@ -250,7 +255,9 @@ const char* dmuon_status_string(int status);
                           only as the next polynomial's aux term). */
 #define DMUON_BUF_R_OPERAND 2 /* the operand copy of the same R / A that the products read
                                  (bf16 on tensor cores, the fp32 buffer otherwise): both
-                                 triangles, bitwise symmetric */
+                                 triangles, bitwise symmetric.  With DMUON_ENGINE_TC_SPLIT
+                                 each row is [hi | lo], each part ld / 2 elements: hi =
+                                 bf16(R), lo = bf16(R - hi) from column ld / 2 on */
 
 /* No counterpart in the paper (test inspection of the symmetric operands of
  * section 2.2).  Byte offset into the bound workspace, leading dimension (elements), batch

@@ -16,7 +16,7 @@ import ctypes
 from . import _lib
 from ._lib import (  # noqa: F401
     BF16, FP32, PREC_BF16, PREC_FP32, ROUTE_AUTO, ROUTE_GRAM, ROUTE_DIRECT, BUCKET_GRAM, BUCKET_DIRECT,
-    ENGINE_TC_BF16, ENGINE_SIMT_FP32, SCALE_ASPECT, SCALE_RMS, TIMER_NAMES, ASSIGN_GREEDY, ASSIGN_EXACT, DmuonError,
+    ENGINE_TC_BF16, ENGINE_SIMT_FP32, ENGINE_TC_SPLIT, SCALE_ASPECT, SCALE_RMS, TIMER_NAMES, ASSIGN_GREEDY, ASSIGN_EXACT, DmuonError,
 )
 
 __all__ = ["Muon", "dmuon_plan", "dmuon_step", "assign_owners", "adamw_step", "load"]

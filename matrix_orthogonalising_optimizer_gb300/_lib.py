@@ -13,7 +13,7 @@ BF16, FP32 = 0, 1
 PREC_BF16, PREC_FP32 = 0, 1
 ROUTE_AUTO, ROUTE_GRAM, ROUTE_DIRECT = 0, 1, 2
 BUCKET_GRAM, BUCKET_DIRECT = 1, 2
-ENGINE_TC_BF16, ENGINE_SIMT_FP32 = 0, 1
+ENGINE_TC_BF16, ENGINE_SIMT_FP32, ENGINE_TC_SPLIT = 0, 1, 2
 SCALE_ASPECT, SCALE_RMS = 0, 1
 OK = 0
 ERR_INVALID_ARG, ERR_ALIGN, ERR_NO_WORKSPACE, ERR_UNSUPPORTED_DTYPE = -1, -2, -3, -4

@@ -4,9 +4,9 @@ The DMuon pages choose work from measured costs rather than FLOP counts
 (technical summary, section 2.3) and tune their kernels per shape (section
 2.4).  Here the choice tuned is each bucket's Newton-Schulz form.  The AUTO
 rule picks Gram space where the bf16 Gram recurrence is accurate enough (n >=
-3m, or small m with fp32 m x m products); the direct form is accurate for
-every shape, so where AUTO picks Gram both forms are candidates, and
-elsewhere direct is the only one.  Each candidate is timed as a step over a
+3m, or small m with split-bf16 m x m products); the direct form is accurate
+for every shape with m >= 128, so where AUTO picks Gram both forms are
+candidates there, Gram alone below, and elsewhere direct is the only one.  Each candidate is timed as a step over a
 sample of matrices of the bucket's shape (seeded synthetic data, CUDA events
 on the stream), and the faster is kept.
 
@@ -29,15 +29,24 @@ __all__ = ["candidates", "cache_key", "autotune_routes"]
 _DT_NAMES = {BF16: "bf16", FP32: "fp32"}
 
 
+# Below this short side the bf16 direct iteration's error reaches the 3e-2
+# bar on O (emulated: 0.025-0.037 for m = 64, at most 0.025 from m = 128 on),
+# so a measured choice never sends such a bucket there.
+DIRECT_MIN_M = 128
+
+
 def candidates(m: int, n: int, precision: str = "bf16", small_m: int = 0) -> list:
     """Routes a bucket of canonical shape (m, n) may take: the AUTO rule's choice and,
-    where that is Gram, also direct (the header's AUTO rule, restated)."""
+    where that is Gram and m >= DIRECT_MIN_M, also direct (the header's AUTO rule,
+    restated)."""
     if small_m == 0:
         small_m = 256
     if precision == "fp32":
         return ["gram", "direct"]
     auto_gram = n >= 3 * m or (small_m > 0 and m <= small_m)
-    return ["gram", "direct"] if auto_gram else ["direct"]
+    if not auto_gram:
+        return ["direct"]
+    return ["gram", "direct"] if m >= DIRECT_MIN_M else ["gram"]
 
 
 def cache_key(m: int, n: int, dtype: str, precision: str, ns_steps: int) -> str:

@@ -35,6 +35,12 @@ uint64_t up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
 
 int esz(int32_t t) { return t == ELEM_BF16 ? 2 : 4; }
 
+// Row length of a split m x m operand [hi | lo]: two parts of m rounded up
+// to the 64-deep K slab.
+int64_t split_ld(int64_t m) { return 2 * static_cast<int64_t>(up(static_cast<uint64_t>(m), 64)); }
+
+bool split_operand(int k) { return k == BUF_RB || k == BUF_P || k == BUF_Q0 || k == BUF_Q1 || k == BUF_RP; }
+
 // ------------------------------------------------------------ template kinds
 
 enum Tmpl : int {
@@ -61,6 +67,11 @@ void bucket_buffers(Bucket& b, int32_t precision) {
         if (b.engine == DMUON_ENGINE_TC_BF16) {
             set(BUF_RF, m * ldm, ELEM_F32);
             for (int k : {BUF_RB, BUF_P, BUF_Q0, BUF_Q1, BUF_RP}) set(k, m * ldm, ELEM_BF16);
+        } else if (b.engine == DMUON_ENGINE_TC_SPLIT) {
+            // fp32 R (aux of P); split operands [hi | lo], each part a whole
+            // number of 64-deep K slabs
+            set(BUF_RF, m * ldm, ELEM_F32);
+            for (int k : {BUF_RB, BUF_P, BUF_Q0, BUF_Q1, BUF_RP}) set(k, m * split_ld(m), ELEM_BF16);
         } else {
             for (int k : {BUF_RF, BUF_P, BUF_Q0, BUF_Q1, BUF_RP}) set(k, m * ldm, ELEM_F32);
             if (precision == DMUON_PREC_BF16) set(BUF_QB, m * ldm, ELEM_BF16);
@@ -127,6 +138,8 @@ struct GroupSpec {
     int kernel = kKernelTc;
     Operand a, b;
     int64_t M = 0, N = 0, K = 0, batch = 0;
+    int64_t kseg = 0;        // K segments (split operands); 0 = none
+    int64_t a_k = 0, b_k = 0;  // K extent of A's / B's tensor map when it differs from K
     bool b_mn = false, sym = false;
     int32_t mode = EPI_STORE, alpha = ALPHA_ONE;
     float c_acc = 1.0f, c_diag = 0.0f, c_aux = 0.0f;
@@ -134,6 +147,7 @@ struct GroupSpec {
     bool aux_sym = false;
     Operand out[3];
     bool out_lower_only[3] = {false, false, false};  // symmetric D: skip the mirror of this output
+    int64_t out_lo[3] = {0, 0, 0};                  // split bf16 output: offset of the low parts
     int64_t slot_base = 0;
 };
 
@@ -152,6 +166,7 @@ int build_group(const GroupSpec& s, GemmGroup* g) {
     g->K = static_cast<int32_t>(s.K);
     g->batch = static_cast<int32_t>(s.batch);
     g->b_mn_major = s.b_mn ? 1 : 0;
+    g->kseg = static_cast<int32_t>(s.kseg);
     g->sym = s.sym ? 1 : 0;
     g->slot_base = static_cast<int32_t>(s.slot_base);
     g->mode = s.mode;
@@ -170,6 +185,7 @@ int build_group(const GroupSpec& s, GemmGroup* g) {
         g->out_ld[o] = static_cast<int32_t>(s.out[o].ld);
         g->out_bs[o] = s.out[o].bs;
         g->out_mirror[o] = s.sym && !s.out_lower_only[o] ? 1 : 0;
+        g->out_lo[o] = static_cast<int32_t>(s.out_lo[o]);
     }
     if (s.kernel == kKernelTc) {
         // pair tiles: 256 rows (two CTAs of 128) x 256 columns
@@ -183,13 +199,14 @@ int build_group(const GroupSpec& s, GemmGroup* g) {
         }
         if (s.a.type != ELEM_BF16 || s.b.type != ELEM_BF16)
             return fail(DMUON_ERR_INVALID_ARG, "internal: tensor-core operands must be bf16");
-        int rc = encode_bf16(&g->tma_a, s.a.p, s.K, s.M, s.batch, s.a.ld, s.a.bs, kTcSlabBytes / 2, kTcBM);
+        const int64_t ak = s.a_k ? s.a_k : s.K, bk = s.b_k ? s.b_k : s.K;
+        int rc = encode_bf16(&g->tma_a, s.a.p, ak, s.M, s.batch, s.a.ld, s.a.bs, kTcSlabBytes / 2, kTcBM);
         if (rc) return rc;
         if (!s.b_mn)
-            rc = encode_bf16(&g->tma_b, s.b.p, s.K, s.N, s.batch, s.b.ld, s.b.bs, kTcSlabBytes / 2,
+            rc = encode_bf16(&g->tma_b, s.b.p, bk, s.N, s.batch, s.b.ld, s.b.bs, kTcSlabBytes / 2,
                              kTcBN / kTcPair);
         else
-            rc = encode_bf16(&g->tma_b, s.b.p, s.N, s.K, s.batch, s.b.ld, s.b.bs, 64, kTcSlabBytes / 2);
+            rc = encode_bf16(&g->tma_b, s.b.p, s.N, bk, s.batch, s.b.ld, s.b.bs, 64, kTcSlabBytes / 2);
         if (rc) return rc;
     } else {
         g->tiles_m = static_cast<int32_t>((s.M + kSimtBM - 1) / kSimtBM);
@@ -318,6 +335,7 @@ static const std::vector<std::vector<Launch>>& launches_for(dmuon_plan_s* h, int
                         const GemmGroup& g = h->groups[gs[j]];
                         l.idx[l.n] = gs[j];
                         l.begin[l.n] = static_cast<int32_t>(tiles);
+                        if (g.out_lo[0] | g.out_lo[1] | g.out_lo[2]) l.has_split = 1;
                         tiles += static_cast<int64_t>(g.tiles_per_mat) * g.batch;
                         ++l.n;
                     }
@@ -438,7 +456,7 @@ dmuon_handle_t dmuon_plan_ex(const dmuon_shape_t* shapes, int64_t count, const d
         const bool small = h->small_m > 0 && b.m <= h->small_m;
         b.route = std::get<3>(kv.first);
         if (h->precision == DMUON_PREC_FP32) b.engine = DMUON_ENGINE_SIMT_FP32;
-        else if (b.route == DMUON_BUCKET_GRAM && small) b.engine = DMUON_ENGINE_SIMT_FP32;
+        else if (b.route == DMUON_BUCKET_GRAM && small) b.engine = DMUON_ENGINE_TC_SPLIT;
         else b.engine = DMUON_ENGINE_TC_BF16;
         bucket_buffers(b, h->precision);
         b.slot0 = slot;
@@ -607,7 +625,7 @@ int dmuon_plan_flops(dmuon_handle_t h, int32_t ns_steps, double* out) {
             cube = T * m * m * m;
         }
         total += cnt * (rect + cube);
-        if (h->precision == DMUON_PREC_BF16) tc += cnt * (rect + (b.engine == DMUON_ENGINE_TC_BF16 ? cube : 0.0));
+        if (h->precision == DMUON_PREC_BF16) tc += cnt * (rect + (b.engine != DMUON_ENGINE_SIMT_FP32 ? cube : 0.0));
     }
     out[0] = total;
     out[1] = tc;
@@ -663,6 +681,7 @@ int dmuon_bind_workspace(dmuon_handle_t h, void* dev_ptr, size_t bytes) {
         o.bs = b.buf_bytes[k] / esz(o.type);
         const bool mm = !(k == BUF_X0 || k == BUF_X1 || k == BUF_PART);
         o.ld = static_cast<int64_t>(up(static_cast<uint64_t>(mm ? b.m : b.n), 8));
+        if (b.engine == DMUON_ENGINE_TC_SPLIT && split_operand(k)) o.ld = split_ld(b.m);
         return o;
     };
 
@@ -707,7 +726,11 @@ int dmuon_bind_workspace(dmuon_handle_t h, void* dev_ptr, size_t bytes) {
             const Bucket& b = h->buckets[p.bucket];
             p.tmpl.assign(TMPL_COUNT, -1);
             const int64_t m = b.m, n = b.n;
-            const int eng = b.engine == DMUON_ENGINE_TC_BF16 ? kKernelTc : kKernelSimt;
+            const int eng = b.engine == DMUON_ENGINE_SIMT_FP32 ? kKernelSimt : kKernelTc;
+            // split engine: every m x m operand stored [hi | lo] (parts of sp
+            // elements); an m x m product runs over K = 3 sp, the final over 2 sp
+            const bool split = b.engine == DMUON_ENGINE_TC_SPLIT;
+            const int64_t sp = split ? split_ld(m) / 2 : 0;
             auto add = [&](int kind, GroupSpec s) -> int {
                 s.batch = p.count;
                 s.slot_base = p.slot0;
@@ -726,7 +749,18 @@ int dmuon_bind_workspace(dmuon_handle_t h, void* dev_ptr, size_t bytes) {
                 s.N = m;
                 s.K = m;
                 s.sym = true;
+                if (split) {
+                    s.K = 3 * sp;
+                    s.kseg = sp;
+                    s.a_k = s.b_k = 2 * sp;
+                }
                 return s;
+            };
+            // split engine: the bf16 m x m outputs are stored [hi | lo]
+            auto split_outputs = [&](GroupSpec& s) {
+                if (!split) return;
+                for (int o = 0; o < 3; ++o)
+                    if (s.out[o].p && s.out[o].type == ELEM_BF16) s.out_lo[o] = sp;
             };
             if (b.route == DMUON_BUCKET_GRAM) {
                 const Operand X0 = buf(p, BUF_X0), RF = buf(p, BUF_RF), RB = buf(p, BUF_RB), P = buf(p, BUF_P),
@@ -747,6 +781,7 @@ int dmuon_bind_workspace(dmuon_handle_t h, void* dev_ptr, size_t bytes) {
                         s.out[1] = RB;
                         s.out_lower_only[0] = true;  // fp32 R: only the next P's aux, lower triangle
                     }
+                    split_outputs(s);
                     if ((rc = add(G_SYRK, s))) return rc;
                 }
                 for (int first = 1; first >= 0; --first) {  // P = aI + bR + cR^2
@@ -761,17 +796,20 @@ int dmuon_bind_workspace(dmuon_handle_t h, void* dev_ptr, size_t bytes) {
                         s.out[1] = Q0;
                         if (QB.p) s.out[2] = QB;
                     }
+                    split_outputs(s);
                     if ((rc = add(first ? G_POLY0 : G_POLY, s))) return rc;
                 }
                 for (int dir = 0; dir < 2; ++dir) {  // Q <- P Q
                     GroupSpec s = sym_spec(eng, P, dir == 0 ? Q0 : Q1);
                     s.out[0] = dir == 0 ? Q1 : Q0;
                     if (QB.p) s.out[1] = QB;
+                    split_outputs(s);
                     if ((rc = add(dir == 0 ? G_Q01 : G_Q10, s))) return rc;
                 }
                 {  // R P
                     GroupSpec s = sym_spec(eng, Rop, P);
                     s.out[0] = RP;
+                    split_outputs(s);
                     if ((rc = add(G_RP, s))) return rc;
                 }
                 {  // R <- P (R P)
@@ -781,6 +819,7 @@ int dmuon_bind_workspace(dmuon_handle_t h, void* dev_ptr, size_t bytes) {
                         s.out[1] = RB;
                         s.out_lower_only[0] = true;
                     }
+                    split_outputs(s);
                     if ((rc = add(G_RUPD, s))) return rc;
                 }
                 for (int qb = 0; qb < 2; ++qb) {  // W update from inv * Q X
@@ -794,6 +833,12 @@ int dmuon_bind_workspace(dmuon_handle_t h, void* dev_ptr, size_t bytes) {
                     s.K = m;
                     s.mode = EPI_UPDATE;
                     s.alpha = ALPHA_INV;
+                    if (split) {  // (Q_hi + Q_lo) X0: K over both parts of Q, X0's rows twice
+                        s.K = 2 * sp;
+                        s.kseg = sp;
+                        s.a_k = 2 * sp;
+                        s.b_k = m;
+                    }
                     if ((rc = add(qb == 0 ? G_FIN0 : G_FIN1, s))) return rc;
                 }
             } else {
@@ -851,6 +896,19 @@ int dmuon_bind_workspace(dmuon_handle_t h, void* dev_ptr, size_t bytes) {
             }
         }
     }
+
+    // split operands: the pad columns between m and each part's end are read
+    // as K data by the products and written by nothing, so they are zeroed
+    // once here
+    for (const Wave& w : h->waves)
+        for (const Piece& p : w.pieces) {
+            const Bucket& b = h->buckets[p.bucket];
+            if (b.engine != DMUON_ENGINE_TC_SPLIT || b.m % 64 == 0) continue;
+            for (int k = 0; k < BUF_COUNT; ++k)
+                if (split_operand(k) && b.buf_bytes[k] &&
+                    cudaMemset(wbase + p.off[k], 0, static_cast<size_t>(p.count * b.buf_bytes[k])) != cudaSuccess)
+                    return fail(DMUON_ERR_CUDA, "split operand clear failed");
+        }
 
     // upload: status + tables
     if (cudaMemset(ws, 0, h->off_infos) != cudaSuccess ||
@@ -1005,6 +1063,7 @@ int dmuon_debug_buffer(dmuon_handle_t h, int64_t wave, int64_t piece, int32_t wh
     if (k < 0 || !b.buf_bytes[k]) return fail(DMUON_ERR_INVALID_ARG, "unknown buffer");
     *offset = h->off_waves + p.off[k];
     *ld = static_cast<int64_t>(up(static_cast<uint64_t>(k == BUF_X0 ? b.n : b.m), 8));
+    if (b.engine == DMUON_ENGINE_TC_SPLIT && split_operand(k)) *ld = split_ld(b.m);
     if (elem_type) *elem_type = b.buf_type[k] == ELEM_BF16 ? DMUON_BF16 : DMUON_FP32;
     *batch_stride = b.buf_bytes[k] / esz(b.buf_type[k]);
     return DMUON_OK;

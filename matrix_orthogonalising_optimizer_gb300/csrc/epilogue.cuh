@@ -76,7 +76,7 @@ struct EpiRegs {
     char* w;
     float alpha, c_acc, c_diag, c_aux, lrs, decay;
     int32_t M, N, mode, sym, aux_type, aux_sym, aux_ld, w_type, w_cols, transposed, w_vec;
-    int32_t out_ld[3], out_type[3], out_mirror[3];
+    int32_t out_ld[3], out_type[3], out_mirror[3], out_lo[3];
 };
 
 __device__ __forceinline__ EpiRegs load_epi(const GemmGroup& g, const LaunchList& L, int mat) {
@@ -89,6 +89,7 @@ __device__ __forceinline__ EpiRegs load_epi(const GemmGroup& g, const LaunchList
         e.out_ld[o] = g.out_ld[o];
         e.out_type[o] = g.out_type[o];
         e.out_mirror[o] = g.sym && g.out_mirror[o];
+        e.out_lo[o] = g.out_lo[o];
     }
     e.w = static_cast<char*>(c.w);
     e.alpha = c.alpha;
@@ -110,6 +111,17 @@ __device__ __forceinline__ EpiRegs load_epi(const GemmGroup& g, const LaunchList
     // 16-byte row access to W needs every row start on 16 bytes
     e.w_vec = c.w && ((static_cast<int64_t>(c.w_cols) * (c.w_type == ELEM_BF16 ? 2 : 4)) % 16 == 0);
     return e;
+}
+
+// The low bf16 part of v: v - bf16(v), exact in fp32, so hi + lo carries v
+// to about 16 significant bits.
+__device__ __forceinline__ float lo_part(float v) { return v - __bfloat162float(__float2bfloat16_rn(v)); }
+
+// Element i of output o (and, for a split output, its low part out_lo
+// elements further along the row).
+__device__ __forceinline__ void store_out(const EpiRegs& e, int o, int64_t i, float v) {
+    store_elem(e.out[o], i, e.out_type[o], v);
+    if (e.out_lo[o]) store_elem(e.out[o], i + e.out_lo[o], ELEM_BF16, lo_part(v));
 }
 
 // Same formula, same operation order as epi_value (epilogue.cuh).
@@ -141,9 +153,8 @@ __device__ __forceinline__ void epi_element_regs(const EpiRegs& e, int r, int co
 #pragma unroll
     for (int o = 0; o < 3; ++o) {
         if (!e.out[o]) continue;
-        store_elem(e.out[o], static_cast<int64_t>(r) * e.out_ld[o] + col, e.out_type[o], v);
-        if (e.out_mirror[o] && r > col)
-            store_elem(e.out[o], static_cast<int64_t>(col) * e.out_ld[o] + r, e.out_type[o], v);
+        store_out(e, o, static_cast<int64_t>(r) * e.out_ld[o] + col, v);
+        if (e.out_mirror[o] && r > col) store_out(e, o, static_cast<int64_t>(col) * e.out_ld[o] + r, v);
     }
 }
 

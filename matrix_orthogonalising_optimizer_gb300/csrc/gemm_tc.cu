@@ -370,35 +370,44 @@ __device__ __forceinline__ void quad_transpose(T (&w)[16], int lane) {
 
 // fp32 rows are transposed in v itself (no copy: the registers are scarce);
 // `restore` transposes v back for later uses.
-__device__ __forceinline__ void st_rows(char* base, int32_t type, int64_t ld, int r0, int c0, int lane,
-                                        float (&v)[CH], int M, bool restore) {
-    if (type == ELEM_BF16) {
-        uint32_t w[8];
+// A bf16 output stored split (lo > 0) writes its low parts lo elements
+// further along each row, with the same lane exchange.
+__device__ __forceinline__ void st_rows_bf16(char* base, int64_t ld, int r0, int c0, int lane, const float (&v)[CH],
+                                             int M, bool low) {
+    uint32_t w[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) w[k] = pack_bf16x2(v[2 * k], v[2 * k + 1]);
-        const bool odd = lane & 1;
-        uint32_t d0[4], d1[4];
+    for (int k = 0; k < 8; ++k)
+        w[k] = low ? pack_bf16x2(lo_part(v[2 * k]), lo_part(v[2 * k + 1])) : pack_bf16x2(v[2 * k], v[2 * k + 1]);
+    const bool odd = lane & 1;
+    uint32_t d0[4], d1[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const uint32_t keep = odd ? w[4 + k] : w[k];
-            const uint32_t recv = __shfl_xor_sync(kFullMask, odd ? w[k] : w[4 + k], 1);
-            d0[k] = odd ? recv : keep;  // row (lane & ~1), half `odd`
-            d1[k] = odd ? keep : recv;  // row (lane | 1),  half `odd`
-        }
-        const int ra = r0 + (lane & ~1);
-        __nv_bfloat16* p = reinterpret_cast<__nv_bfloat16*>(base) + static_cast<int64_t>(ra) * ld + c0 + 8 * odd;
-        if (ra < M) *reinterpret_cast<uint4*>(p) = make_uint4(d0[0], d0[1], d0[2], d0[3]);
-        if (ra + 1 < M) *reinterpret_cast<uint4*>(p + ld) = make_uint4(d1[0], d1[1], d1[2], d1[3]);
-    } else {
-        quad_transpose(v, lane);
-        const int rq = r0 + (lane & ~3);
-        float* p = reinterpret_cast<float*>(base) + static_cast<int64_t>(rq) * ld + c0 + 4 * (lane & 3);
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            if (rq + j < M)
-                *reinterpret_cast<float4*>(p + j * ld) = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-        if (restore) quad_transpose(v, lane);
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t keep = odd ? w[4 + k] : w[k];
+        const uint32_t recv = __shfl_xor_sync(kFullMask, odd ? w[k] : w[4 + k], 1);
+        d0[k] = odd ? recv : keep;  // row (lane & ~1), half `odd`
+        d1[k] = odd ? keep : recv;  // row (lane | 1),  half `odd`
     }
+    const int ra = r0 + (lane & ~1);
+    __nv_bfloat16* p = reinterpret_cast<__nv_bfloat16*>(base) + static_cast<int64_t>(ra) * ld + c0 + 8 * odd;
+    if (ra < M) *reinterpret_cast<uint4*>(p) = make_uint4(d0[0], d0[1], d0[2], d0[3]);
+    if (ra + 1 < M) *reinterpret_cast<uint4*>(p + ld) = make_uint4(d1[0], d1[1], d1[2], d1[3]);
+}
+
+__device__ __forceinline__ void st_rows(char* base, int32_t type, int64_t ld, int r0, int c0, int lane,
+                                        float (&v)[CH], int M, bool restore, int lo) {
+    if (type == ELEM_BF16) {
+        st_rows_bf16(base, ld, r0, c0, lane, v, M, false);
+        if (lo) st_rows_bf16(base + 2 * static_cast<int64_t>(lo), ld, r0, c0, lane, v, M, true);
+        return;
+    }
+    quad_transpose(v, lane);
+    const int rq = r0 + (lane & ~3);
+    float* p = reinterpret_cast<float*>(base) + static_cast<int64_t>(rq) * ld + c0 + 4 * (lane & 3);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        if (rq + j < M)
+            *reinterpret_cast<float4*>(p + j * ld) = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    if (restore) quad_transpose(v, lane);
 }
 
 __device__ __forceinline__ void ld_rows(const char* base, int32_t type, int64_t ld, int r0, int c0, int lane,
@@ -535,9 +544,10 @@ __device__ __forceinline__ void epi_load(const EpiRegs& e, int r, int r0, int la
 // columns, like quad_transpose one level deeper), so lane (g, t) =
 // (lane / 8, lane % 8) ends with mirrored rows t and 8 + t, columns
 // r0 + 8g .. r0 + 8g + 7, as two 16-byte bf16 pieces: two stores per lane
-// instead of sixteen 2-byte ones.  v is left as it is.  All 32 lanes must call
-// this.
-__device__ __forceinline__ void mirror_words(const float (&v)[CH], int lane, uint4 (&mw)[2]) {
+// instead of sixteen 2-byte ones; with `low`, the pieces hold the low bf16
+// parts of a split output instead.  v is left as it is.  All 32 lanes must
+// call this.
+__device__ __forceinline__ void mirror_words(const float (&v)[CH], int lane, uint4 (&mw)[2], bool low) {
     float a[CH];
 #pragma unroll
     for (int j = 0; j < CH; ++j) a[j] = v[j];
@@ -557,6 +567,10 @@ __device__ __forceinline__ void mirror_words(const float (&v)[CH], int lane, uin
             }
         }
     }
+    if (low) {
+#pragma unroll
+        for (int j = 0; j < CH; ++j) a[j] = lo_part(a[j]);
+    }
 #pragma unroll
     for (int h = 0; h < 2; ++h)
         mw[h] = make_uint4(pack_bf16x2(a[8 * h], a[8 * h + 1]), pack_bf16x2(a[8 * h + 2], a[8 * h + 3]),
@@ -572,6 +586,9 @@ __device__ __forceinline__ void st_mirror(char* base, int64_t ld, int r0, int c0
 
 // v (computed in place of the accumulator values) and, for the update, the new
 // W (in place of the loaded W values), to keep the register footprint low.
+// kSplit: the launch holds groups with split outputs (the other instance
+// carries none of their code).
+template <bool kSplit>
 __device__ __forceinline__ void epi_finish(const EpiRegs& e, int r, int r0, int lane, int c0, float (&v)[CH],
                                            float (&x)[CH]) {
     if (r0 >= e.M) return;  // warp-uniform: no row of this warp exists
@@ -607,27 +624,41 @@ __device__ __forceinline__ void epi_finish(const EpiRegs& e, int r, int r0, int 
 #pragma unroll
         for (int o = 2; o >= 0; --o) {
             if (!e.out[o]) continue;
+            const int lo = kSplit ? e.out_lo[o] : 0;
             if (e.out_mirror[o]) {
-                if (mfast && e.out_type[o] == ELEM_BF16 && (e.out_ld[o] & 7) == 0) {  // warp-uniform
+                if (mfast && e.out_type[o] == ELEM_BF16 && ((e.out_ld[o] | lo) & 7) == 0) {  // warp-uniform
                     if (!have_mw) {
-                        mirror_words(v, lane, mw);
+                        mirror_words(v, lane, mw, false);
                         have_mw = true;
                     }
                     st_mirror(e.out[o], e.out_ld[o], r0, c0, lane, mw);
+                    if (lo) {
+                        // low parts in the same registers (the high parts are
+                        // rebuilt for a later split output)
+                        mirror_words(v, lane, mw, true);
+                        st_mirror(e.out[o] + 2 * static_cast<int64_t>(lo), e.out_ld[o], r0, c0, lane, mw);
+                        have_mw = false;
+                    }
                 } else if (valid) {
 #pragma unroll
                     for (int j = 0; j < CH; ++j)
-                        if (j < ncol && r > c0 + j)
-                            store_elem(e.out[o], static_cast<int64_t>(c0 + j) * e.out_ld[o] + r, e.out_type[o], v[j]);
+                        if (j < ncol && r > c0 + j) {
+                            const int64_t i = static_cast<int64_t>(c0 + j) * e.out_ld[o] + r;
+                            store_elem(e.out[o], i, e.out_type[o], v[j]);
+                            if (lo) store_elem(e.out[o], i + lo, ELEM_BF16, lo_part(v[j]));
+                        }
                 }
             }
             if (coop) {
-                st_rows(e.out[o], e.out_type[o], e.out_ld[o], r0, c0, lane, v, e.M, o > 0);
+                st_rows(e.out[o], e.out_type[o], e.out_ld[o], r0, c0, lane, v, e.M, o > 0, lo);
             } else if (valid) {
                 const int64_t rb = static_cast<int64_t>(r) * e.out_ld[o];
 #pragma unroll
                 for (int j = 0; j < CH; ++j)
-                    if (j < ncol && (!e.sym || r >= c0 + j)) store_elem(e.out[o], rb + c0 + j, e.out_type[o], v[j]);
+                    if (j < ncol && (!e.sym || r >= c0 + j)) {
+                        store_elem(e.out[o], rb + c0 + j, e.out_type[o], v[j]);
+                        if (lo) store_elem(e.out[o], rb + lo + c0 + j, ELEM_BF16, lo_part(v[j]));
+                    }
             }
         }
         return;
@@ -639,7 +670,7 @@ __device__ __forceinline__ void epi_finish(const EpiRegs& e, int r, int r0, int 
     if (!e.transposed) {
         const int64_t rb = static_cast<int64_t>(r) * e.w_cols;
         if (full && e.w_vec) {
-            st_rows(e.w, e.w_type, e.w_cols, r0, c0, lane, w, e.M, false);
+            st_rows(e.w, e.w_type, e.w_cols, r0, c0, lane, w, e.M, false, 0);
         } else if (valid) {
 #pragma unroll
             for (int j = 0; j < CH; ++j)
@@ -732,6 +763,7 @@ __device__ __forceinline__ void tw_store(const EpiRegs& e, int c0, int q, int wc
     }
 }
 
+template <bool kSplit>
 __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_constant__ LaunchList L) {
     extern __shared__ uint8_t smem_raw[];
     Smem& S = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -805,6 +837,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
             const GemmGroup* g = L.groups + L.idx[tc.gi];
             const int nkb = (g->K + SLAB_K - 1) / SLAB_K;
             const int b_col = tc.tn * BN + rank * (BN / kPair);  // this CTA's 128 columns of B
+            // per-tile fields in registers (the waits' memory clobbers would
+            // otherwise reload them from the group table for every slab)
+            const int kseg = g->kseg;
+            const bool b_mn = g->b_mn_major != 0;
+            const CUtensorMap* map_a = &g->tma_a;
+            const CUtensorMap* map_b = &g->tma_b;
             for (int kb = 0; kb < nkb; ++kb) {
                 if (!mbar_wait(&S.empty[stage], phase ^ 1, L.status)) {
                     ok = false;
@@ -816,14 +854,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
                 // own 128 rows of A and own 128 columns of B, counted on the
                 // leader's barrier
                 const uint32_t fb = mapa(saddr(&S.full[stage]), 0);
-                tma_load_3d_pair(S.a[stage], &g->tma_a, fb, kb * SLAB_K, (2 * tc.tm + rank) * BM, tc.mat);
-                if (!g->b_mn_major) {
-                    tma_load_3d_pair(S.b[stage], &g->tma_b, fb, kb * SLAB_K, b_col, tc.mat);
+                // K coordinates of this slab in A and in B (split operands:
+                // segment t of K reads A's segment t % 2, B's t / 2)
+                int ka = kb * SLAB_K, kbk = ka;
+                if (kseg > 0) {
+                    const int seg = ka / kseg, within = ka - seg * kseg;
+                    ka = (seg & 1) * kseg + within;
+                    kbk = (seg >> 1) * kseg + within;
+                }
+                tma_load_3d_pair(S.a[stage], map_a, fb, ka, (2 * tc.tm + rank) * BM, tc.mat);
+                if (!b_mn) {
+                    tma_load_3d_pair(S.b[stage], map_b, fb, kbk, b_col, tc.mat);
                 } else {
 #pragma unroll
                     for (int i = 0; i < BN / 64 / kPair; ++i)
-                        tma_load_3d_pair(S.b[stage] + i * MN_BOX_BYTES, &g->tma_b, fb, b_col + 64 * i, kb * SLAB_K,
-                                         tc.mat);
+                        tma_load_3d_pair(S.b[stage] + i * MN_BOX_BYTES, map_b, fb, b_col + 64 * i, kbk, tc.mat);
                 }
                 if (++stage == STAGES) {
                     stage = 0;
@@ -972,7 +1017,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
                 float v[CH];
                 __syncwarp();
                 tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN + (ch0 + kc) * CH), v);
-                epi_finish(e, r, r0w, lane, c0, v, x);
+                epi_finish<kSplit>(e, r, r0w, lane, c0, v, x);
             }
             }
             tc_fence_before();
@@ -1015,17 +1060,20 @@ cudaError_t launch_gemm_tc(const LaunchList& l, int num_sms, cudaStream_t s) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    // the shared-memory attribute is set, and the resident pairs counted, once
-    // per device with that device current
+    // the shared-memory attribute is set (on both instances), and the resident
+    // pairs counted, once per device with that device current
     int max_pairs = 0;
     e = max_pairs_per_device.get(dev, &max_pairs, [&](int* out) {
-        cudaError_t r = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t r = cudaFuncSetAttribute(gemm_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(gemm_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(smem));
         if (r != cudaSuccess) return r;
         cudaLaunchConfig_t probe = cfg;
         probe.gridDim = dim3(num_sms / kPair * kPair);
         int n = 0;
-        r = cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel, &probe);
+        r = cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<false>, &probe);
         if (r != cudaSuccess) return r;
         *out = n > 0 ? n : num_sms / kPair;
         return cudaSuccess;
@@ -1033,7 +1081,8 @@ cudaError_t launch_gemm_tc(const LaunchList& l, int num_sms, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     const int pairs = l.total_tiles < max_pairs ? l.total_tiles : max_pairs;
     cfg.gridDim = dim3(pairs * kPair);
-    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, l);
+    if (l.has_split) return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<true>, l);
+    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<false>, l);
 }
 
 }  // namespace dmuon

@@ -76,6 +76,12 @@ struct GemmGroup {
     int32_t a_type, b_type; // ElemType
     int32_t M, N, K, batch;
     int32_t b_mn_major;
+    // K split into segments of kseg elements (a multiple of the 64-deep slab;
+    // 0 = one segment): K slab j of segment t reads A at segment t % 2 and B
+    // at segment t / 2 of their rows.  With operands stored as [hi | lo]
+    // (bf16 x = hi + lo) and K = 3 kseg this accumulates hi*hi + lo*hi +
+    // hi*lo; with K = 2 kseg and a plain B it accumulates (hi + lo) * B.
+    int32_t kseg;
     int32_t sym;            // symmetric D: lower-triangle tiles, mirrored stores
     int32_t tiles_m, tiles_n, tiles_per_mat;
     int32_t slot_base;      // slot of batch entry 0
@@ -94,6 +100,8 @@ struct GemmGroup {
     int32_t out_ld[3];
     int32_t out_type[3];
     int32_t out_mirror[3];  // symmetric D: also store the upper triangle of this output
+    int32_t out_lo[3];      // bf16 output stored split: hi = bf16(v) at column c, lo = bf16(v - hi)
+                            // at column out_lo + c of the same row (0 = plain)
 };
 
 // Passed by value to every GEMM launch.
@@ -107,6 +115,7 @@ struct LaunchList {
     float lr, decay;                         // update: W = decay*W - lr*s*v
     int32_t n;                               // groups in this launch
     int32_t total_tiles;
+    int32_t has_split;                       // some group stores split outputs (tcgen05 kernel instance)
     int32_t idx[kMaxGroupsPerLaunch];        // indices into `groups`
     int32_t begin[kMaxGroupsPerLaunch + 1];  // tile prefix
 };

@@ -14,8 +14,9 @@ C ABI header ``include/dmuon.h`` states for ``dmuon_plan``:
   FP32 precision -> Gram unless the rule is DIRECT; AUTO -> Gram when
   n >= 3m or m <= small_m, else direct;
 * buckets keyed (dtype, m, n, route), ascending;
-* m x m engine: FP32 precision -> fp32 FFMA; BF16 precision -> fp32 FFMA for
-  Gram buckets with m <= small_m, tensor cores otherwise;
+* m x m engine: FP32 precision -> fp32 FFMA; BF16 precision -> split-bf16
+  tensor cores for Gram buckets with m <= small_m, plain bf16 tensor cores
+  otherwise;
 * per-matrix workspace bytes: the sum of the per-matrix buffers below, each
   rounded up to 256 bytes;
 * waves: buckets packed greedily in bucket order under the budget, a bucket
@@ -30,7 +31,7 @@ BF16, FP32 = 0, 1
 PREC_BF16, PREC_FP32 = 0, 1
 ROUTE_AUTO, ROUTE_GRAM, ROUTE_DIRECT = 0, 1, 2
 BUCKET_GRAM, BUCKET_DIRECT = 1, 2
-ENGINE_TC_BF16, ENGINE_SIMT_FP32 = 0, 1
+ENGINE_TC_BF16, ENGINE_SIMT_FP32, ENGINE_TC_SPLIT = 0, 1, 2
 
 
 def _up(x: int, a: int) -> int:
@@ -44,6 +45,9 @@ def per_matrix_bytes(m: int, n: int, precision: int, route: int, engine: int) ->
     if route == BUCKET_GRAM:
         if engine == ENGINE_TC_BF16:
             bufs += [m * ldm * 4] + [m * ldm * 2] * 5      # Rf; Rb, P, Q0, Q1, RP
+        elif engine == ENGINE_TC_SPLIT:
+            # Rf; R, P, Q0, Q1, RP as bf16 rows [hi | lo], each part m rounded up to 64
+            bufs += [m * ldm * 4] + [m * 2 * _up(m, 64) * 2] * 5
         else:
             bufs += [m * ldm * 4] * 5                      # R, P, Q0, Q1, RP
             if precision == PREC_BF16:
@@ -87,7 +91,7 @@ def plan_buckets(shapes, precision: int = PREC_BF16, route: int = ROUTE_AUTO,
         if precision == PREC_FP32:
             eng = ENGINE_SIMT_FP32
         elif r == BUCKET_GRAM and small_m > 0 and m <= small_m:
-            eng = ENGINE_SIMT_FP32
+            eng = ENGINE_TC_SPLIT
         else:
             eng = ENGINE_TC_BF16
         buckets.append({"dtype": dtype, "m": m, "n": n, "members": keyed[key], "route": r,

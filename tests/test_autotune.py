@@ -16,7 +16,8 @@ import oracle
 
 def test_candidates_follow_the_planner_rule():
     # the AUTO route (the oracle planner's restatement) is always a candidate,
-    # direct is always a candidate, and Gram only where AUTO picks it
+    # Gram only where AUTO picks it, and direct except where AUTO picks Gram
+    # for a bf16 bucket of m < 128 (direct bf16 iteration too inaccurate there)
     rng = random.Random(0)
     for _ in range(300):
         r, c = rng.randint(1, 5000), rng.randint(1, 5000)
@@ -26,8 +27,9 @@ def test_candidates_follow_the_planner_rule():
                 b, _ = oplan.plan_buckets([(r, c, 0)], precision=pcode, small_m=small)
                 auto = "gram" if b[0]["route"] == oplan.BUCKET_GRAM else "direct"
                 cand = candidates(m, n, prec, small)
-                assert auto in cand and "direct" in cand
+                assert auto in cand
                 assert ("gram" in cand) == (auto == "gram")
+                assert ("direct" in cand) == (auto == "direct" or prec == "fp32" or m >= 128)
 
 
 def test_cache_and_choice_with_a_fake_timer(tmp_path):

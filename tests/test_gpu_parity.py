@@ -185,35 +185,48 @@ def test_deterministic_and_batching_invariant():
 
 
 def test_symmetric_operands_bitwise():
-    # The R / A that the products read (bf16 on tensor cores, fp32 for the
-    # FFMA engine) is stored as lower triangle plus mirror: bitwise symmetric.
-    # The fp32 copy kept for the next polynomial's aux term holds the same
-    # lower triangle before rounding.
+    # The R / A that the products read (bf16 on tensor cores; split into
+    # [hi | lo] bf16 parts for small m) is stored as lower triangle plus
+    # mirror: bitwise symmetric.  The fp32 copy kept for the next polynomial's
+    # aux term holds the same lower triangle before rounding.  An fp32 mode
+    # plan checks the FFMA engine's fp32 operand the same way.
     shapes = [(320, 704)] * 2 + [(300, 960)] + [(520, 1100)] + [(100, 400)] * 2
     inputs = make_inputs(shapes, "bf16", 20)
     _, _, muon = run_step(shapes, inputs, "bf16", lr=LR, beta=BETA, wd=WD)
     ws = muon.workspace
     buckets = muon.buckets()
-    assert {b["route"] for b in buckets} == {1, 2} and {b["engine"] for b in buckets} == {0, 1}
+    assert {b["route"] for b in buckets} == {1, 2} and {b["engine"] for b in buckets} == {0, 2}
+    _check_symmetric_operands(muon, ws, buckets)
+    _, _, m32 = run_step(shapes, inputs, "bf16", lr=LR, beta=BETA, wd=WD, precision="fp32")
+    assert {b["engine"] for b in m32.buckets()} == {1}
+    _check_symmetric_operands(m32, m32.workspace, m32.buckets())
 
-    def matrices(p, which, m, nb):
+
+def _check_symmetric_operands(muon, ws, buckets):
+    def matrices(p, which, m, nb, col0=0):
         off, ld, bs, dt = muon.debug_buffer(0, p, which)
         tdt, esz = (torch.bfloat16, 2) if dt == "bf16" else (torch.float32, 4)
         raw = ws[off: off + nb * bs * esz].view(tdt).cpu().view(nb, bs)
-        return [raw[j, : m * ld].view(m, ld)[:, :m] for j in range(nb)], dt
+        return [raw[j, : m * ld].view(m, ld)[:, col0:col0 + m] for j in range(nb)], dt, ld
 
     for p, (bi, start, nb) in enumerate(muon.waves()[0]):
         m = buckets[bi]["m"]
-        ops, dt = matrices(p, 2, m, nb)
-        fps, _ = matrices(p, 1, m, nb)
+        ops, dt, ld = matrices(p, 2, m, nb)
+        fps, _, _ = matrices(p, 1, m, nb)
+        split = buckets[bi]["engine"] == 2
+        los = matrices(p, 2, m, nb, ld // 2)[0] if split else [None] * nb
         low = torch.tril(torch.ones(m, m, dtype=torch.bool))
-        for op, fp in zip(ops, fps):
+        for op, fp, lo in zip(ops, fps, los):
             assert torch.equal(op, op.t())
             assert torch.isfinite(op.float()).all()
             if dt == "bf16":
                 assert torch.equal(fp.to(torch.bfloat16)[low], op[low])
             else:
                 assert torch.equal(fp, op)
+            if split:
+                # lo = bf16(R - hi), R - hi exact in fp32; symmetric like hi
+                assert torch.equal(lo, lo.t())
+                assert torch.equal((fp - op.float()).to(torch.bfloat16)[low], lo[low])
 
 
 def test_workspace_budget_waves():
@@ -238,7 +251,8 @@ def test_timing_counts_launches():
     run_step(shapes, inputs, "bf16", lr=LR, beta=BETA, wd=WD, muon=muon)
     t = muon.timing()
     assert t["momentum"][1] == 1 and t["norm"][1] == 1
-    assert t["tc"][1] > 0 and t["simt"][1] > 0
+    # bf16 mode: every product on tensor cores (small m through split operands)
+    assert t["tc"][1] > 0 and t["simt"][1] == 0
     assert all(v[0] >= 0 for v in t.values())
 
 

@@ -329,6 +329,19 @@ def test_plan_per_matrix_bytes_hand_worked():
     assert oplan.per_matrix_bytes(m, n, oplan.PREC_BF16, oplan.BUCKET_GRAM, oplan.ENGINE_TC_BF16) == want
 
 
+def test_plan_per_matrix_bytes_split_engine_hand_worked():
+    # m=100, n=700 bf16 Gram bucket with split m x m operands: ldn = 704,
+    # ldm = 104; each split operand row is [hi | lo] with both parts 128 long
+    # u: 100*704*2 = 140800 -> 140800 (550 * 256); Rf: 100*104*4 = 41600 -> 41728;
+    # five split operands: 100*256*2 = 51200 (= 200 * 256) each;
+    # partials: 2 x 11 tiles, 8 floats each: 704 -> 768
+    want = 140800 + 41728 + 5 * 51200 + 768
+    assert oplan.per_matrix_bytes(100, 700, oplan.PREC_BF16, oplan.BUCKET_GRAM, oplan.ENGINE_TC_SPLIT) == want
+    b, _ = oplan.plan_buckets([(700, 100, 0)])
+    assert (b[0]["route"], b[0]["engine"], b[0]["per_matrix_bytes"]) == (oplan.BUCKET_GRAM, oplan.ENGINE_TC_SPLIT,
+                                                                        want)
+
+
 def test_plan_waves_split_buckets():
     shapes = [(64, 64, 0)] * 5 + [(64, 128, 0)] * 3
     b0, _ = oplan.plan_buckets(shapes)
@@ -355,7 +368,7 @@ def test_plan_fp32_and_forced_routes():
     b, _ = oplan.plan_buckets([(600, 700, 0), (200, 210, 0)], small_m=-1)
     assert [x["route"] for x in b] == [oplan.BUCKET_DIRECT, oplan.BUCKET_DIRECT]
     b, _ = oplan.plan_buckets([(600, 700, 0), (200, 210, 0)])
-    assert [(x["route"], x["engine"]) for x in b] == [(oplan.BUCKET_GRAM, oplan.ENGINE_SIMT_FP32),
+    assert [(x["route"], x["engine"]) for x in b] == [(oplan.BUCKET_GRAM, oplan.ENGINE_TC_SPLIT),
                                                       (oplan.BUCKET_DIRECT, oplan.ENGINE_TC_BF16)]
 
 
