@@ -341,6 +341,13 @@ static const std::vector<std::vector<Launch>>& launches_for(dmuon_plan_s* h, int
                     }
                     l.begin[l.n] = static_cast<int32_t>(tiles);
                     l.total_tiles = static_cast<int32_t>(tiles);
+                    // the tcgen05 kernel's shared stage serves the transposed
+                    // update or diagonal store chunks: never both in one launch
+                    for (int j = 1; j < l.n; ++j)
+                        if (h->groups[l.idx[j]].mode != h->groups[l.idx[0]].mode) {
+                            fail(DMUON_ERR_INVALID_ARG, "internal: a launch mixes update and store products");
+                            h->phase_error = true;
+                        }
                     char* ws = h->ws;
                     l.groups = reinterpret_cast<const GemmGroup*>(ws + h->off_groups);
                     l.infos = reinterpret_cast<const MatInfo*>(ws + h->off_infos);
@@ -968,6 +975,7 @@ int dmuon_step_ex(dmuon_handle_t h, void* const* params, const void* const* grad
     }
 
     const auto& per_wave = launches_for(h, ns_steps);
+    if (h->phase_error) return DMUON_ERR_INVALID_ARG;
     void* const* dptr = reinterpret_cast<void* const*>(h->ws + h->off_ptrs);
     bool waited = params_ready == nullptr;
     const float decay = 1.0f - lr * wd;

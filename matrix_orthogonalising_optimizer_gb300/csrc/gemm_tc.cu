@@ -60,6 +60,7 @@ constexpr uint32_t TMEM_COLS = 512;             // two 256-column accumulators
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr int kTileRing = 4;
 constexpr int kTStageLd = 132;  // 128 W columns + 4 pad; 528-byte rows keep float4 reads aligned
+static_assert(4 * 32 * 16 <= 16 * kTStageLd, "a half's stage holds four 32 x 16 diagonal slices");
 constexpr int kEpiWarps = (kTcThreads - 64) / 32;
 // epilogue warps come in sets of four (one per TMEM lane quarter); each set
 // takes an equal part of the 256 accumulator columns
@@ -83,7 +84,8 @@ struct __align__(1024) Smem {
     int32_t tile_slot[kTileRing];
     uint32_t tmem_base;
     // transposed W update: a 16 x 128 chunk of v per column half, padded rows
-    // (read as float4: 16-byte aligned)
+    // (read as float4: 16-byte aligned); in store launches four 32 x 16
+    // slices per half, one per epilogue warp, stage diagonal chunks
     alignas(16) float tstage[2][CH * kTStageLd];
 };
 
@@ -373,7 +375,7 @@ __device__ __forceinline__ void quad_transpose(T (&w)[16], int lane) {
 // A bf16 output stored split (lo > 0) writes its low parts lo elements
 // further along each row, with the same lane exchange.
 __device__ __forceinline__ void st_rows_bf16(char* base, int64_t ld, int r0, int c0, int lane, const float (&v)[CH],
-                                             int M, bool low) {
+                                             int M, bool low, int rmin) {
     uint32_t w[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k)
@@ -389,15 +391,17 @@ __device__ __forceinline__ void st_rows_bf16(char* base, int64_t ld, int r0, int
     }
     const int ra = r0 + (lane & ~1);
     __nv_bfloat16* p = reinterpret_cast<__nv_bfloat16*>(base) + static_cast<int64_t>(ra) * ld + c0 + 8 * odd;
-    if (ra < M) *reinterpret_cast<uint4*>(p) = make_uint4(d0[0], d0[1], d0[2], d0[3]);
-    if (ra + 1 < M) *reinterpret_cast<uint4*>(p + ld) = make_uint4(d1[0], d1[1], d1[2], d1[3]);
+    if (ra < M && ra >= rmin) *reinterpret_cast<uint4*>(p) = make_uint4(d0[0], d0[1], d0[2], d0[3]);
+    if (ra + 1 < M && ra + 1 >= rmin) *reinterpret_cast<uint4*>(p + ld) = make_uint4(d1[0], d1[1], d1[2], d1[3]);
 }
 
+// Rows below rmin are not stored (the upper half of a chunk right of the
+// diagonal).
 __device__ __forceinline__ void st_rows(char* base, int32_t type, int64_t ld, int r0, int c0, int lane,
-                                        float (&v)[CH], int M, bool restore, int lo) {
+                                        float (&v)[CH], int M, bool restore, int lo, int rmin = 0) {
     if (type == ELEM_BF16) {
-        st_rows_bf16(base, ld, r0, c0, lane, v, M, false);
-        if (lo) st_rows_bf16(base + 2 * static_cast<int64_t>(lo), ld, r0, c0, lane, v, M, true);
+        st_rows_bf16(base, ld, r0, c0, lane, v, M, false, rmin);
+        if (lo) st_rows_bf16(base + 2 * static_cast<int64_t>(lo), ld, r0, c0, lane, v, M, true, rmin);
         return;
     }
     quad_transpose(v, lane);
@@ -405,7 +409,7 @@ __device__ __forceinline__ void st_rows(char* base, int32_t type, int64_t ld, in
     float* p = reinterpret_cast<float*>(base) + static_cast<int64_t>(rq) * ld + c0 + 4 * (lane & 3);
 #pragma unroll
     for (int j = 0; j < 4; ++j)
-        if (rq + j < M)
+        if (rq + j < M && rq + j >= rmin)
             *reinterpret_cast<float4*>(p + j * ld) = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
     if (restore) quad_transpose(v, lane);
 }
@@ -584,13 +588,87 @@ __device__ __forceinline__ void st_mirror(char* base, int64_t ld, int r0, int c0
     *reinterpret_cast<uint4*>(p + static_cast<int64_t>(c0 + 8 + t) * ld) = mw[1];
 }
 
+// A whole 32 x 16 chunk of a symmetric result that touches the diagonal
+// (c0 == r0: rows r0 .. r0+15 hold the 16 x 16 diagonal block, rows
+// r0+16 .. r0+31 lie below it; c0 == r0 + 16: rows r0+16 .. hold the
+// diagonal block, rows r0 .. r0+15 lie above it).  Instead of element-wise
+// stores of the lower triangle and its mirror (one 2-byte store per lane and
+// element, each to another row), the chunk is staged in `stg` (512 floats of
+// shared memory owned by this warp, XOR-swizzled rows) and written back as
+// 8-element row pieces, one per lane and pass, each a 16-byte (bf16) or two
+// 16-byte (fp32) stores:
+//   - rows of the chunk (all 32 for c0 == r0, the lower 16 otherwise), with
+//     the diagonal block as the symmetric result holds it: element (r, c)
+//     is acc[r][c] on and below the diagonal and acc[c][r] above it;
+//   - for c0 == r0, the mirror of the rows below the block: rows c0 .. c0+15,
+//     columns r0+16 .. r0+31.
+// Every upper element is still the mirror of a lower one: the result stays
+// bitwise symmetric.  All 32 lanes must call this.
+__device__ __forceinline__ int stg_idx(int i, int j) { return i * CH + (j ^ (i & 15)); }
+
+// 8 consecutive elements from (row r0 + i, column c0 + j0) of output o.
+template <bool kSplit>
+__device__ __forceinline__ void st_piece(const EpiRegs& e, int o, int64_t idx, const float (&w)[8]) {
+    const int lo = kSplit ? e.out_lo[o] : 0;
+    if (e.out_type[o] == ELEM_BF16) {
+        __nv_bfloat16* p = reinterpret_cast<__nv_bfloat16*>(e.out[o]) + idx;
+        *reinterpret_cast<uint4*>(p) = make_uint4(pack_bf16x2(w[0], w[1]), pack_bf16x2(w[2], w[3]),
+                                                  pack_bf16x2(w[4], w[5]), pack_bf16x2(w[6], w[7]));
+        if (lo)
+            *reinterpret_cast<uint4*>(p + lo) =
+                make_uint4(pack_bf16x2(lo_part(w[0]), lo_part(w[1])), pack_bf16x2(lo_part(w[2]), lo_part(w[3])),
+                           pack_bf16x2(lo_part(w[4]), lo_part(w[5])), pack_bf16x2(lo_part(w[6]), lo_part(w[7])));
+    } else {
+        float4* p = reinterpret_cast<float4*>(reinterpret_cast<float*>(e.out[o]) + idx);
+        p[0] = make_float4(w[0], w[1], w[2], w[3]);
+        p[1] = make_float4(w[4], w[5], w[6], w[7]);
+    }
+}
+
+template <bool kSplit>
+__device__ __forceinline__ void epi_store_diag(const EpiRegs& e, int r0, int lane, int c0, const float (&v)[CH],
+                                               float* stg) {
+#pragma unroll
+    for (int j = 0; j < CH; ++j) stg[stg_idx(lane, j)] = v[j];
+    __syncwarp();
+    const int d = c0 - r0;  // 0 or 16: the diagonal block's first row inside the chunk
+    const int h = lane & 1;
+    // rows: pass 1 for the block rows d .. d+15, pass 0 (c0 == r0 only) for rows 16 .. 31
+#pragma unroll
+    for (int pass = 0; pass < 2; ++pass) {
+        if (pass == 0 && d != 0) continue;
+        const int i = (pass == 0 ? 16 : d) + (lane >> 1);  // chunk row
+        float w[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            const int j = 8 * h + t;  // chunk column; matrix column c0 + j vs row r0 + i
+            w[t] = (pass == 1 && j + d > i) ? stg[stg_idx(j + d, i - d)] : stg[stg_idx(i, j)];
+        }
+#pragma unroll
+        for (int o = 2; o >= 0; --o)
+            if (e.out[o]) st_piece<kSplit>(e, o, static_cast<int64_t>(r0 + i) * e.out_ld[o] + c0 + 8 * h, w);
+    }
+    if (d == 0) {
+        // mirrored row c0 + (lane >> 1), columns r0 + 16 + 8h .. : chunk rows 16 + 8h ..
+        const int jj = lane >> 1, i0 = 16 + 8 * h;
+        float w[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) w[t] = stg[stg_idx(i0 + t, jj)];
+#pragma unroll
+        for (int o = 2; o >= 0; --o)
+            if (e.out[o] && e.out_mirror[o])
+                st_piece<kSplit>(e, o, static_cast<int64_t>(c0 + jj) * e.out_ld[o] + r0 + i0, w);
+    }
+    __syncwarp();  // the stage is read before the next chunk writes it
+}
+
 // v (computed in place of the accumulator values) and, for the update, the new
 // W (in place of the loaded W values), to keep the register footprint low.
 // kSplit: the launch holds groups with split outputs (the other instance
 // carries none of their code).
 template <bool kSplit>
 __device__ __forceinline__ void epi_finish(const EpiRegs& e, int r, int r0, int lane, int c0, float (&v)[CH],
-                                           float (&x)[CH]) {
+                                           float (&x)[CH], float* stg) {
     if (r0 >= e.M) return;  // warp-uniform: no row of this warp exists
     const bool valid = r < e.M;
     const int ncol = min(CH, e.N - c0);
@@ -612,6 +690,13 @@ __device__ __forceinline__ void epi_finish(const EpiRegs& e, int r, int r0, int 
     }
 
     if (!upd) {
+        if (e.sym && c0 + CH - 1 >= r0) {  // warp-uniform: the chunk reaches the warp's diagonal
+            if (c0 >= r0 + 32) return;     // wholly above it: nothing of it is stored
+            if (full && r0 + 32 <= e.M) {
+                epi_store_diag<kSplit>(e, r0, lane, c0, v, stg);
+                return;
+            }
+        }
         // every column of the chunk is stored directly in all 32 rows of the warp
         const bool coop = full && (!e.sym || c0 + CH - 1 < r0);
         // whole 32-row chunk left of the diagonal block: bf16 mirrors built
@@ -1004,6 +1089,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
                     named_bar(1 + half);  // the chunk is read before the next one is staged
                 }
             } else {
+            // this warp's 32 x 16 staging slice for diagonal chunks (the
+            // transposed-update stage: a launch holds store groups or update
+            // groups, never both)
+            float* stg = S.tstage[half] + q * (32 * CH);
             float xin[CH];
             if (nch > 0) epi_load(e, r, r0w, lane, tc.tn * BN + ch0 * CH, xin);
             if (!mbar_wait_cluster(&S.acc_full[buf], use & 1, L.status)) break;
@@ -1017,7 +1106,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
                 float v[CH];
                 __syncwarp();
                 tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN + (ch0 + kc) * CH), v);
-                epi_finish<kSplit>(e, r, r0w, lane, c0, v, x);
+                epi_finish<kSplit>(e, r, r0w, lane, c0, v, x, stg);
             }
             }
             tc_fence_before();

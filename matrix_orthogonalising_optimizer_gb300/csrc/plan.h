@@ -103,6 +103,7 @@ struct dmuon_plan_s {
     std::vector<int> group_kernel;        // per group: 0 tcgen05, 1 fp32 FFMA
     std::vector<const void*> cached_ptrs;  // params | grads | momenta
     std::map<int, std::vector<std::vector<dmuon::Launch>>> phase_cache;  // ns_steps -> per wave
+    bool phase_error = false;              // a launch table broke an invariant (message set)
 
     // timing
     bool timing = false;
