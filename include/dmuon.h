@@ -80,6 +80,11 @@ extern "C" {
                                    product hi*hi + hi*lo + lo*hi; the final product's Q
                                    as hi + lo */
 
+/* tile rules of the tensor-core symmetric products of buckets with m <= 128 */
+#define DMUON_TILE_PACKED 0   /* 2 (m <= 128) or 4 (m <= 64) matrices per 256 x 256 pair
+                                 tile, laid block-diagonally */
+#define DMUON_TILE_SINGLE 1   /* one matrix per pair tile */
+
 /* update-scale rules */
 #define DMUON_SCALE_ASPECT 0 /* s = sqrt(max(1, rows/cols)) */
 #define DMUON_SCALE_RMS 1    /* s = 0.2*sqrt(max(rows, cols)) */
@@ -122,7 +127,7 @@ typedef struct {
     int32_t small_m;        /* AUTO route and BF16 mode: Gram buckets with m <= small_m run
                                their m x m products on split-bf16 tensor cores
                                (DMUON_ENGINE_TC_SPLIT); 0 => 256; < 0 => none */
-    int32_t reserved;
+    int32_t tile_rule;      /* DMUON_TILE_*; default PACKED */
     uint64_t workspace_budget; /* bytes for one wave of buckets; 0 => everything in one wave */
 } dmuon_options_t;
 

@@ -16,7 +16,7 @@ import ctypes
 from . import _lib
 from ._lib import (  # noqa: F401
     BF16, FP32, PREC_BF16, PREC_FP32, ROUTE_AUTO, ROUTE_GRAM, ROUTE_DIRECT, BUCKET_GRAM, BUCKET_DIRECT,
-    ENGINE_TC_BF16, ENGINE_SIMT_FP32, ENGINE_TC_SPLIT, SCALE_ASPECT, SCALE_RMS, TIMER_NAMES, ASSIGN_GREEDY, ASSIGN_EXACT, DmuonError,
+    ENGINE_TC_BF16, ENGINE_SIMT_FP32, ENGINE_TC_SPLIT, TILE_PACKED, TILE_SINGLE, SCALE_ASPECT, SCALE_RMS, TIMER_NAMES, ASSIGN_GREEDY, ASSIGN_EXACT, DmuonError,
 )
 
 __all__ = ["Muon", "dmuon_plan", "dmuon_step", "assign_owners", "adamw_step", "load"]
@@ -25,6 +25,7 @@ _DTYPES = {"bf16": BF16, "fp32": FP32}
 _PREC = {"bf16": PREC_BF16, "fp32": PREC_FP32}
 _ROUTES = {"auto": ROUTE_AUTO, "gram": ROUTE_GRAM, "direct": ROUTE_DIRECT}
 _SCALES = {"aspect": SCALE_ASPECT, "rms": SCALE_RMS}
+_TILES = {"packed": TILE_PACKED, "single": TILE_SINGLE}
 
 
 def load():
@@ -41,7 +42,7 @@ def _stream_handle(stream):
 
 
 def dmuon_plan(shapes, dtype="bf16", precision="bf16", route="auto", coeffs=None, eps=0.0,
-               scale_rule="aspect", nesterov=True, small_m=0, workspace_budget=0):
+               scale_rule="aspect", nesterov=True, small_m=0, workspace_budget=0, tile="packed"):
     """dmuon_plan_ex: shapes is a list of (rows, cols[, dtype[, route]]); a shape's route
     ("auto" / 0 = the plan's ``route``, "gram", "direct") overrides the plan's rule."""
     lib = _lib.load()
@@ -61,6 +62,7 @@ def dmuon_plan(shapes, dtype="bf16", precision="bf16", route="auto", coeffs=None
     opt.scale_rule = _SCALES[scale_rule]
     opt.no_nesterov = 0 if nesterov else 1
     opt.small_m = small_m
+    opt.tile_rule = _TILES[tile]
     opt.workspace_budget = workspace_budget
     h = lib.dmuon_plan_ex(arr, len(shapes), ctypes.byref(opt))
     if not h:

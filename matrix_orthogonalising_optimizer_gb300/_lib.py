@@ -14,6 +14,7 @@ PREC_BF16, PREC_FP32 = 0, 1
 ROUTE_AUTO, ROUTE_GRAM, ROUTE_DIRECT = 0, 1, 2
 BUCKET_GRAM, BUCKET_DIRECT = 1, 2
 ENGINE_TC_BF16, ENGINE_SIMT_FP32, ENGINE_TC_SPLIT = 0, 1, 2
+TILE_PACKED, TILE_SINGLE = 0, 1
 SCALE_ASPECT, SCALE_RMS = 0, 1
 OK = 0
 ERR_INVALID_ARG, ERR_ALIGN, ERR_NO_WORKSPACE, ERR_UNSUPPORTED_DTYPE = -1, -2, -3, -4
@@ -31,7 +32,7 @@ class Shape(ctypes.Structure):
 class Options(ctypes.Structure):
     _fields_ = [("precision", c_int32), ("route", c_int32), ("ns_a", c_float), ("ns_b", c_float),
                 ("ns_c", c_float), ("eps", c_float), ("scale_rule", c_int32), ("no_nesterov", c_int32),
-                ("small_m", c_int32), ("reserved", c_int32), ("workspace_budget", c_uint64)]
+                ("small_m", c_int32), ("tile_rule", c_int32), ("workspace_budget", c_uint64)]
 
 
 class BucketInfo(ctypes.Structure):

@@ -115,11 +115,11 @@ int get_encoder() {
 
 // bf16 rank-3 view {dim0 (contiguous), dim1, batch}, 128-byte swizzle.
 int encode_bf16(CUtensorMap* map, const void* base, int64_t dim0, int64_t dim1, int64_t batch, int64_t ld,
-                int64_t bs, uint32_t box0, uint32_t box1) {
+                int64_t bs, uint32_t box0, uint32_t box1, uint32_t box2) {
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(dim0), static_cast<cuuint64_t>(dim1),
                           static_cast<cuuint64_t>(batch)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld * 2), static_cast<cuuint64_t>(bs * 2)};
-    cuuint32_t box[3] = {box0, box1, 1};
+    cuuint32_t box[3] = {box0, box1, box2};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -151,7 +151,7 @@ struct GroupSpec {
     int64_t slot_base = 0;
 };
 
-int build_group(const GroupSpec& s, GemmGroup* g) {
+int build_group(const GroupSpec& s, GemmGroup* g, int32_t tile_rule) {
     std::memset(g, 0, sizeof(*g));
     g->a = s.a.p;
     g->b = s.b.p;
@@ -187,6 +187,7 @@ int build_group(const GroupSpec& s, GemmGroup* g) {
         g->out_mirror[o] = s.sym && !s.out_lower_only[o] ? 1 : 0;
         g->out_lo[o] = static_cast<int32_t>(s.out_lo[o]);
     }
+    g->pack = 1;
     if (s.kernel == kKernelTc) {
         // pair tiles: 256 rows (two CTAs of 128) x 256 columns
         const int64_t pair_rows = kTcPair * kTcBM;
@@ -197,22 +198,29 @@ int build_group(const GroupSpec& s, GemmGroup* g) {
         } else {
             g->tiles_per_mat = g->tiles_m * g->tiles_n;
         }
+        // small symmetric products: several matrices block-diagonally per tile
+        if (s.sym && tile_rule == DMUON_TILE_PACKED && s.M <= kTcBM) g->pack = s.M <= kTcBM / 2 ? 4 : 2;
         if (s.a.type != ELEM_BF16 || s.b.type != ELEM_BF16)
             return fail(DMUON_ERR_INVALID_ARG, "internal: tensor-core operands must be bf16");
         const int64_t ak = s.a_k ? s.a_k : s.K, bk = s.b_k ? s.b_k : s.K;
-        int rc = encode_bf16(&g->tma_a, s.a.p, ak, s.M, s.batch, s.a.ld, s.a.bs, kTcSlabBytes / 2, kTcBM);
+        // a CTA's 128 rows of A (and of K-major B): one matrix's rows, or two
+        // 64-row matrices of a tile packed by four
+        const uint32_t rows = g->pack == 4 ? kTcBM / 2 : kTcBM, mats = g->pack == 4 ? 2 : 1;
+        int rc = encode_bf16(&g->tma_a, s.a.p, ak, s.M, s.batch, s.a.ld, s.a.bs, kTcSlabBytes / 2, rows, mats);
         if (rc) return rc;
         if (!s.b_mn)
             rc = encode_bf16(&g->tma_b, s.b.p, bk, s.N, s.batch, s.b.ld, s.b.bs, kTcSlabBytes / 2,
-                             kTcBN / kTcPair);
+                             g->pack > 1 ? rows : kTcBN / kTcPair, mats);
         else
-            rc = encode_bf16(&g->tma_b, s.b.p, s.N, bk, s.batch, s.b.ld, s.b.bs, 64, kTcSlabBytes / 2);
+            rc = encode_bf16(&g->tma_b, s.b.p, s.N, bk, s.batch, s.b.ld, s.b.bs, 64, kTcSlabBytes / 2, 1);
         if (rc) return rc;
     } else {
         g->tiles_m = static_cast<int32_t>((s.M + kSimtBM - 1) / kSimtBM);
         g->tiles_n = static_cast<int32_t>((s.N + kSimtBN - 1) / kSimtBN);
         g->tiles_per_mat = s.sym ? g->tiles_m * (g->tiles_m + 1) / 2 : g->tiles_m * g->tiles_n;
     }
+    g->ntiles = g->pack > 1 ? static_cast<int32_t>((s.batch + g->pack - 1) / g->pack)
+                            : static_cast<int32_t>(g->tiles_per_mat * s.batch);
     return DMUON_OK;
 }
 
@@ -336,7 +344,7 @@ static const std::vector<std::vector<Launch>>& launches_for(dmuon_plan_s* h, int
                         l.idx[l.n] = gs[j];
                         l.begin[l.n] = static_cast<int32_t>(tiles);
                         if (g.out_lo[0] | g.out_lo[1] | g.out_lo[2]) l.has_split = 1;
-                        tiles += static_cast<int64_t>(g.tiles_per_mat) * g.batch;
+                        tiles += g.ntiles;
                         ++l.n;
                     }
                     l.begin[l.n] = static_cast<int32_t>(tiles);
@@ -407,7 +415,8 @@ dmuon_handle_t dmuon_plan_ex(const dmuon_shape_t* shapes, int64_t count, const d
         return nullptr;
     }
     if (!(o.eps >= 0.0f) || !std::isfinite(o.eps) || !std::isfinite(o.ns_a) || !std::isfinite(o.ns_b) ||
-        !std::isfinite(o.ns_c) || (o.no_nesterov != 0 && o.no_nesterov != 1) || o.reserved != 0) {
+        !std::isfinite(o.ns_c) || (o.no_nesterov != 0 && o.no_nesterov != 1) ||
+        (o.tile_rule != DMUON_TILE_PACKED && o.tile_rule != DMUON_TILE_SINGLE)) {
         fail(DMUON_ERR_INVALID_ARG, "bad option values");
         return nullptr;
     }
@@ -423,6 +432,7 @@ dmuon_handle_t dmuon_plan_ex(const dmuon_shape_t* shapes, int64_t count, const d
     h->scale_rule = o.scale_rule;
     h->nesterov = o.no_nesterov ? 0 : 1;
     h->small_m = o.small_m == 0 ? 256 : o.small_m;
+    h->tile_rule = o.tile_rule;
     h->budget = o.workspace_budget;
     h->count = count;
     h->shapes.assign(shapes, shapes + count);
@@ -741,7 +751,7 @@ int dmuon_bind_workspace(dmuon_handle_t h, void* dev_ptr, size_t bytes) {
             auto add = [&](int kind, GroupSpec s) -> int {
                 s.batch = p.count;
                 s.slot_base = p.slot0;
-                const int rc2 = build_group(s, &h->groups[next]);
+                const int rc2 = build_group(s, &h->groups[next], h->tile_rule);
                 if (rc2) return rc2;
                 gk[next] = s.kernel;
                 p.tmpl[kind] = static_cast<int32_t>(next++);

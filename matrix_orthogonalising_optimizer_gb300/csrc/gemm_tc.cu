@@ -24,7 +24,9 @@
 //               leader one thread issues the MMAs (kind::f16, bf16 operands,
 //               fp32 accumulation) into one of two 256-column accumulators
 //               and commits to both CTAs' barriers
-//   warps 2..9  (both CTAs) epilogue, two per TMEM lane quarter (128 columns
+//   warps 2, 3  idle (they complete warpgroup 0, whose registers go to the
+//               epilogue: setmaxnreg, 56 per thread against 224)
+//   warps 4..11 (both CTAs) epilogue, two per TMEM lane quarter (128 columns
 //               each): tcgen05.ld the accumulator (row per thread), apply the
 //               fused epilogue, store; then release the accumulator to the
 //               leader so the next tile's MMAs overlap this tile's epilogue.
@@ -61,7 +63,18 @@ constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr int kTileRing = 4;
 constexpr int kTStageLd = 132;  // 128 W columns + 4 pad; 528-byte rows keep float4 reads aligned
 static_assert(4 * 32 * 16 <= 16 * kTStageLd, "a half's stage holds four 32 x 16 diagonal slices");
-constexpr int kEpiWarps = (kTcThreads - 64) / 32;
+// warpgroup 0 (warps 0-3): TMA, MMA and two idle warps; warpgroups 1-2:
+// the epilogue
+constexpr int kEpiWarp0 = 4;
+constexpr int kEpiWarps = (kTcThreads - 32 * kEpiWarp0) / 32;
+// Registers per thread after the split (setmaxnreg): warpgroup 0 gives
+// back what its roles do not need, the epilogue takes it.  Per SM
+// sub-partition (one warp of each warpgroup) 56 + 2 x 224 = 3 x 168, the
+// launch's allocation, so the increase never waits for registers that are
+// not there.
+constexpr int kRegsLow = 56;
+constexpr int kRegsEpi = 224;
+static_assert(kTcThreads == 384 && kRegsLow + 2 * kRegsEpi <= 3 * 168, "register split must fit the launch");
 // epilogue warps come in sets of four (one per TMEM lane quarter); each set
 // takes an equal part of the 256 accumulator columns
 constexpr int kColParts = kEpiWarps / 4;
@@ -302,7 +315,7 @@ __device__ __forceinline__ TileCoord decode_tile(const LaunchList& L, int t) {
     const GemmGroup& g = L.groups[L.idx[gi]];
     const int local = t - L.begin[gi];
     c.gi = gi;
-    c.mat = local / g.tiles_per_mat;
+    c.mat = local / g.tiles_per_mat * g.pack;  // packed groups: the tile's first matrix
     int idx = local % g.tiles_per_mat;
     if (g.sym) {
         int i = 0;
@@ -505,11 +518,11 @@ __device__ __forceinline__ void prefetch_rows(const char* base, int32_t type, in
 }
 
 __device__ __forceinline__ void epi_prefetch(const EpiRegs& e, int r, int r0, int lane, int c_first, int ncols) {
-    if (e.mode == EPI_UPDATE) {
-        prefetch_rows(e.w, e.w_type, e.w_cols, e.transposed, r, r0, lane, c_first, ncols, e.M, e.N);
-        if (e.aux) prefetch_rows(e.aux, e.aux_type, e.aux_ld, e.aux_sym, r, r0, lane, c_first, ncols, e.M, e.N);
+    if (e.update()) {
+        prefetch_rows(e.w, e.w_type(), e.w_cols, e.transposed(), r, r0, lane, c_first, ncols, e.M, e.N);
+        if (e.aux) prefetch_rows(e.aux, e.aux_type(), e.aux_ld, e.aux_sym(), r, r0, lane, c_first, ncols, e.M, e.N);
     } else if (e.aux) {
-        prefetch_rows(e.aux, e.aux_type, e.aux_ld, e.aux_sym, r, r0, lane, c_first, ncols, e.M, e.N);
+        prefetch_rows(e.aux, e.aux_type(), e.aux_ld, e.aux_sym(), r, r0, lane, c_first, ncols, e.M, e.N);
     }
 }
 
@@ -522,17 +535,17 @@ __device__ __forceinline__ void epi_load(const EpiRegs& e, int r, int r0, int la
     int32_t type, ld;
     bool by_col;
     bool vec;
-    if (e.mode == EPI_UPDATE) {
+    if (e.update()) {
         base = e.w;
-        type = e.w_type;
+        type = e.w_type();
         ld = e.w_cols;
-        by_col = e.transposed;
-        vec = full && e.w_vec;
+        by_col = e.transposed();
+        vec = full && e.w_vec();
     } else if (e.aux) {
         base = e.aux;
-        type = e.aux_type;
+        type = e.aux_type();
         ld = e.aux_ld;
-        by_col = e.aux_sym;
+        by_col = e.aux_sym();
         vec = full;
     } else {
         return;
@@ -610,7 +623,7 @@ __device__ __forceinline__ int stg_idx(int i, int j) { return i * CH + (j ^ (i &
 template <bool kSplit>
 __device__ __forceinline__ void st_piece(const EpiRegs& e, int o, int64_t idx, const float (&w)[8]) {
     const int lo = kSplit ? e.out_lo[o] : 0;
-    if (e.out_type[o] == ELEM_BF16) {
+    if (e.out_type(o) == ELEM_BF16) {
         __nv_bfloat16* p = reinterpret_cast<__nv_bfloat16*>(e.out[o]) + idx;
         *reinterpret_cast<uint4*>(p) = make_uint4(pack_bf16x2(w[0], w[1]), pack_bf16x2(w[2], w[3]),
                                                   pack_bf16x2(w[4], w[5]), pack_bf16x2(w[6], w[7]));
@@ -656,7 +669,7 @@ __device__ __forceinline__ void epi_store_diag(const EpiRegs& e, int r0, int lan
         for (int t = 0; t < 8; ++t) w[t] = stg[stg_idx(i0 + t, jj)];
 #pragma unroll
         for (int o = 2; o >= 0; --o)
-            if (e.out[o] && e.out_mirror[o])
+            if (e.out[o] && e.out_mirror(o))
                 st_piece<kSplit>(e, o, static_cast<int64_t>(c0 + jj) * e.out_ld[o] + r0 + i0, w);
     }
     __syncwarp();  // the stage is read before the next chunk writes it
@@ -673,15 +686,15 @@ __device__ __forceinline__ void epi_finish(const EpiRegs& e, int r, int r0, int 
     const bool valid = r < e.M;
     const int ncol = min(CH, e.N - c0);
     const bool full = ncol == CH;
-    const bool upd = e.mode == EPI_UPDATE;
+    const bool upd = e.update();
     if (upd && e.aux) {
         // the update that also has an aux term (direct route: a X + B X) reads
         // the aux chunk here; x already holds W
         float a[CH];
 #pragma unroll
         for (int j = 0; j < CH; ++j) a[j] = 0.0f;
-        if (full && !e.aux_sym) ld_rows(e.aux, e.aux_type, e.aux_ld, r0, c0, lane, a, e.M);
-        else if (valid) load_row(e.aux, e.aux_type, e.aux_ld, e.aux_sym, r, c0, ncol, a);
+        if (full && !e.aux_sym()) ld_rows(e.aux, e.aux_type(), e.aux_ld, r0, c0, lane, a, e.M);
+        else if (valid) load_row(e.aux, e.aux_type(), e.aux_ld, e.aux_sym(), r, c0, ncol, a);
 #pragma unroll
         for (int j = 0; j < CH; ++j) v[j] = epi_v(e, r, c0 + j, v[j], a[j]);
     } else {
@@ -690,7 +703,7 @@ __device__ __forceinline__ void epi_finish(const EpiRegs& e, int r, int r0, int 
     }
 
     if (!upd) {
-        if (e.sym && c0 + CH - 1 >= r0) {  // warp-uniform: the chunk reaches the warp's diagonal
+        if (e.sym() && c0 + CH - 1 >= r0) {  // warp-uniform: the chunk reaches the warp's diagonal
             if (c0 >= r0 + 32) return;     // wholly above it: nothing of it is stored
             if (full && r0 + 32 <= e.M) {
                 epi_store_diag<kSplit>(e, r0, lane, c0, v, stg);
@@ -698,10 +711,10 @@ __device__ __forceinline__ void epi_finish(const EpiRegs& e, int r, int r0, int 
             }
         }
         // every column of the chunk is stored directly in all 32 rows of the warp
-        const bool coop = full && (!e.sym || c0 + CH - 1 < r0);
+        const bool coop = full && (!e.sym() || c0 + CH - 1 < r0);
         // whole 32-row chunk left of the diagonal block: bf16 mirrors built
         // once in registers (mirror_words), shared by every mirrored output
-        const bool mfast = coop && e.sym && r0 + 32 <= e.M;
+        const bool mfast = coop && e.sym() && r0 + 32 <= e.M;
         uint4 mw[2];
         bool have_mw = false;
         // last output first, and each output's mirror before its rows: an fp32
@@ -710,8 +723,8 @@ __device__ __forceinline__ void epi_finish(const EpiRegs& e, int r, int r0, int 
         for (int o = 2; o >= 0; --o) {
             if (!e.out[o]) continue;
             const int lo = kSplit ? e.out_lo[o] : 0;
-            if (e.out_mirror[o]) {
-                if (mfast && e.out_type[o] == ELEM_BF16 && ((e.out_ld[o] | lo) & 7) == 0) {  // warp-uniform
+            if (e.out_mirror(o)) {
+                if (mfast && e.out_type(o) == ELEM_BF16 && ((e.out_ld[o] | lo) & 7) == 0) {  // warp-uniform
                     if (!have_mw) {
                         mirror_words(v, lane, mw, false);
                         have_mw = true;
@@ -729,19 +742,19 @@ __device__ __forceinline__ void epi_finish(const EpiRegs& e, int r, int r0, int 
                     for (int j = 0; j < CH; ++j)
                         if (j < ncol && r > c0 + j) {
                             const int64_t i = static_cast<int64_t>(c0 + j) * e.out_ld[o] + r;
-                            store_elem(e.out[o], i, e.out_type[o], v[j]);
+                            store_elem(e.out[o], i, e.out_type(o), v[j]);
                             if (lo) store_elem(e.out[o], i + lo, ELEM_BF16, lo_part(v[j]));
                         }
                 }
             }
             if (coop) {
-                st_rows(e.out[o], e.out_type[o], e.out_ld[o], r0, c0, lane, v, e.M, o > 0, lo);
+                st_rows(e.out[o], e.out_type(o), e.out_ld[o], r0, c0, lane, v, e.M, o > 0, lo);
             } else if (valid) {
                 const int64_t rb = static_cast<int64_t>(r) * e.out_ld[o];
 #pragma unroll
                 for (int j = 0; j < CH; ++j)
-                    if (j < ncol && (!e.sym || r >= c0 + j)) {
-                        store_elem(e.out[o], rb + c0 + j, e.out_type[o], v[j]);
+                    if (j < ncol && (!e.sym() || r >= c0 + j)) {
+                        store_elem(e.out[o], rb + c0 + j, e.out_type(o), v[j]);
                         if (lo) store_elem(e.out[o], rb + lo + c0 + j, ELEM_BF16, lo_part(v[j]));
                     }
             }
@@ -752,19 +765,19 @@ __device__ __forceinline__ void epi_finish(const EpiRegs& e, int r, int r0, int 
     float (&w)[CH] = x;
 #pragma unroll
     for (int j = 0; j < CH; ++j) w[j] = fmaf(-e.lrs, v[j], e.decay * x[j]);
-    if (!e.transposed) {
+    if (!e.transposed()) {
         const int64_t rb = static_cast<int64_t>(r) * e.w_cols;
-        if (full && e.w_vec) {
-            st_rows(e.w, e.w_type, e.w_cols, r0, c0, lane, w, e.M, false, 0);
+        if (full && e.w_vec()) {
+            st_rows(e.w, e.w_type(), e.w_cols, r0, c0, lane, w, e.M, false, 0);
         } else if (valid) {
 #pragma unroll
             for (int j = 0; j < CH; ++j)
-                if (j < ncol) store_elem(e.w, rb + c0 + j, e.w_type, w[j]);
+                if (j < ncol) store_elem(e.w, rb + c0 + j, e.w_type(), w[j]);
         }
     } else if (valid) {
 #pragma unroll
         for (int j = 0; j < CH; ++j)
-            if (j < ncol) store_elem(e.w, static_cast<int64_t>(c0 + j) * e.w_cols + r, e.w_type, w[j]);
+            if (j < ncol) store_elem(e.w, static_cast<int64_t>(c0 + j) * e.w_cols + r, e.w_type(), w[j]);
     }
 }
 
@@ -801,7 +814,7 @@ __device__ __forceinline__ void tw_load(const EpiRegs& e, int c0, int q, int wc,
         if (c >= e.N) continue;
         const int64_t base = static_cast<int64_t>(c) * e.w_cols + wc;
         if (wc + 3 < e.M) {
-            if (e.w_type == ELEM_BF16) {
+            if (e.w_type() == ELEM_BF16) {
                 const uint2 u = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(e.w) + base);
                 const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
                 const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
@@ -813,7 +826,7 @@ __device__ __forceinline__ void tw_load(const EpiRegs& e, int c0, int q, int wc,
         } else {
 #pragma unroll
             for (int t = 0; t < 4; ++t)
-                if (wc + t < e.M) w[i][t] = load_elem(e.w, base + t, e.w_type);
+                if (wc + t < e.M) w[i][t] = load_elem(e.w, base + t, e.w_type());
         }
     }
 }
@@ -831,7 +844,7 @@ __device__ __forceinline__ void tw_store(const EpiRegs& e, int c0, int q, int wc
         const float n3 = fmaf(-e.lrs, v.w, e.decay * w[i][3]);
         const int64_t base = static_cast<int64_t>(c) * e.w_cols + wc;
         if (wc + 3 < e.M) {
-            if (e.w_type == ELEM_BF16) {
+            if (e.w_type() == ELEM_BF16) {
                 uint2 u;
                 *reinterpret_cast<__nv_bfloat162*>(&u.x) = __floats2bfloat162_rn(n0, n1);
                 *reinterpret_cast<__nv_bfloat162*>(&u.y) = __floats2bfloat162_rn(n2, n3);
@@ -843,7 +856,7 @@ __device__ __forceinline__ void tw_store(const EpiRegs& e, int c0, int q, int wc
             const float n[4] = {n0, n1, n2, n3};
 #pragma unroll
             for (int t = 0; t < 4; ++t)
-                if (wc + t < e.M) store_elem(e.w, base + t, e.w_type, n[t]);
+                if (wc + t < e.M) store_elem(e.w, base + t, e.w_type(), n[t]);
         }
     }
 }
@@ -885,6 +898,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     const int rank = static_cast<int>(cluster_rank());
     const int total = L.total_tiles;
 
+    // Register split, warpgroup-uniform; each role's code sits inside the
+    // branch of its own setmaxnreg, so it is compiled to that budget.
+    if (warp < kEpiWarp0) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------ TMA producer
         uint32_t stage = 0, phase = 0;
@@ -926,6 +943,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
             // otherwise reload them from the group table for every slab)
             const int kseg = g->kseg;
             const bool b_mn = g->b_mn_major != 0;
+            // packed group: CTA rank r holds matrices mat + r pack/2 .. (rows 0 ..)
+            const int pk = g->pack;
+            const int a_row = pk > 1 ? 0 : (2 * tc.tm + rank) * BM;
+            const int b_row = pk > 1 ? 0 : b_col;
+            const int zb = pk > 1 ? tc.mat + rank * (pk >> 1) : tc.mat;
             const CUtensorMap* map_a = &g->tma_a;
             const CUtensorMap* map_b = &g->tma_b;
             for (int kb = 0; kb < nkb; ++kb) {
@@ -947,9 +969,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
                     ka = (seg & 1) * kseg + within;
                     kbk = (seg >> 1) * kseg + within;
                 }
-                tma_load_3d_pair(S.a[stage], map_a, fb, ka, (2 * tc.tm + rank) * BM, tc.mat);
+                tma_load_3d_pair(S.a[stage], map_a, fb, ka, a_row, zb);
                 if (!b_mn) {
-                    tma_load_3d_pair(S.b[stage], map_b, fb, kbk, b_col, tc.mat);
+                    tma_load_3d_pair(S.b[stage], map_b, fb, kbk, b_row, zb);
                 } else {
 #pragma unroll
                     for (int i = 0; i < BN / 64 / kPair; ++i)
@@ -1030,10 +1052,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
             // epilogue's wait on it covers them before TMEM is released
             umma_commit_mc(&S.acc_full[buf], kPairMask);
         }
-    } else if (warp >= 2) {
+    }
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsEpi));
         // ------------------------------------------------ epilogue
         const int q = warp & 3;             // TMEM lane quarter this warp may access
-        const int half = (warp - 2) / 4;    // which column part (of kColParts) of the 256 columns
+        const int half = (warp - kEpiWarp0) / 4;  // which column part (of kColParts) of the 256 columns
         int it = 0;
         for (int k = 0;; ++k, ++it) {
             const int t = wait_tile(S.tile_full, S.tile_slot, k, L.status, total);
@@ -1044,34 +1068,49 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
             const GemmGroup& g = L.groups[L.idx[tc.gi]];
             const int buf = it & 1;
             const uint32_t use = static_cast<uint32_t>(it >> 1);
-            const EpiRegs e = load_epi(g, L, tc.mat);
             const int tm = 2 * tc.tm + rank;  // this CTA's 128-row tile
-            const int r0w = tm * BM + q * 32;  // first row of this warp
+            // this warp's matrix, first row, first column (matrix
+            // coordinates) and accumulator column of its chunks
+            constexpr int kHalfCols = BN / kColParts;
+            int mat = tc.mat, r0w = tm * BM + q * 32, cbase = tc.tn * BN + half * kHalfCols;
+            int tcol0 = half * kHalfCols, maxch = kHalfCols / CH, row_last = tm * BM + BM - 1;
+            bool active = true;
+            if (g.pack > 1) {
+                // packed tile: diagonal block pm (mpad x mpad) is matrix
+                // mat + pm; this warp's rows lie in block row / mpad, whose
+                // columns belong to one column half
+                const int mpad = BN / g.pack, row = rank * BM + q * 32, pm = row / mpad;
+                mat = tc.mat + pm;
+                r0w = row - pm * mpad;
+                cbase = 0;
+                tcol0 = pm * mpad;
+                maxch = mpad / CH;
+                row_last = mpad - 1;
+                active = pm * mpad / kHalfCols == half && mat < g.batch;
+            }
+            const EpiRegs e = load_epi(g, L, active ? mat : tc.mat);
             const int r = r0w + lane;
-            const int row_last = tm * BM + BM - 1;
             // chunks of this warp that hold stored columns
-            constexpr int kChunks = (BN / kColParts) / CH;
-            const int ch0 = half * kChunks;
             int nch = 0;
-            for (int ch = ch0; ch < ch0 + kChunks; ++ch) {
-                const int c0 = tc.tn * BN + ch * CH;
-                if (c0 >= e.N || (e.sym && e.mode == EPI_STORE && c0 > row_last)) break;
+            for (int ch = 0; active && ch < maxch; ++ch) {
+                const int c0 = cbase + ch * CH;
+                if (c0 >= e.N || (e.sym() && !e.update() && c0 > row_last)) break;
                 ++nch;
             }
-            if (nch > 0) epi_prefetch(e, r, tm * BM + q * 32, lane, tc.tn * BN + ch0 * CH, nch * CH);
+            if (nch > 0) epi_prefetch(e, r, r0w, lane, cbase, nch * CH);
             // tall matrices' update through the staged path (the same four warps
             // of this half always see the same nch, so the named barriers match)
-            const bool tpath = e.mode == EPI_UPDATE && e.transposed && !e.aux && (e.w_cols % 4) == 0;
+            const bool tpath = e.update() && e.transposed() && !e.aux && (e.w_cols % 4) == 0;
             if (tpath) {
                 const int wc = tm * BM + 4 * lane;
                 float* stg = S.tstage[half];
                 float wn[4][4];
-                if (nch > 0) tw_load(e, tc.tn * BN + ch0 * CH, q, wc, wn);
+                if (nch > 0) tw_load(e, cbase, q, wc, wn);
                 const bool ready = mbar_wait_cluster(&S.acc_full[buf], use & 1, L.status);
                 if (!named_bar_and(1 + half, ready)) break;
                 tc_fence_after();
                 for (int kc = 0; kc < nch; ++kc) {
-                    const int c0 = tc.tn * BN + (ch0 + kc) * CH;
+                    const int c0 = cbase + kc * CH;
                     float wcur[4][4];
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
@@ -1081,7 +1120,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
                     float v[CH];
                     __syncwarp();
                     tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) +
-                                  static_cast<uint32_t>(buf * BN + (ch0 + kc) * CH), v);
+                                  static_cast<uint32_t>(buf * BN + tcol0 + kc * CH), v);
 #pragma unroll
                     for (int j = 0; j < CH; ++j) stg[j * kTStageLd + q * 32 + lane] = epi_v(e, r, c0 + j, v[j], 0.0f);
                     named_bar(1 + half);
@@ -1094,18 +1133,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
             // groups, never both)
             float* stg = S.tstage[half] + q * (32 * CH);
             float xin[CH];
-            if (nch > 0) epi_load(e, r, r0w, lane, tc.tn * BN + ch0 * CH, xin);
+            if (nch > 0) epi_load(e, r, r0w, lane, cbase, xin);
             if (!mbar_wait_cluster(&S.acc_full[buf], use & 1, L.status)) break;
             tc_fence_after();
             for (int kc = 0; kc < nch; ++kc) {
-                const int c0 = tc.tn * BN + (ch0 + kc) * CH;
+                const int c0 = cbase + kc * CH;
                 float x[CH];
 #pragma unroll
                 for (int j = 0; j < CH; ++j) x[j] = xin[j];
                 if (kc + 1 < nch) epi_load(e, r, r0w, lane, c0 + CH, xin);
                 float v[CH];
                 __syncwarp();
-                tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN + (ch0 + kc) * CH), v);
+                tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN + tcol0 + kc * CH), v);
                 epi_finish<kSplit>(e, r, r0w, lane, c0, v, x, stg);
             }
             }

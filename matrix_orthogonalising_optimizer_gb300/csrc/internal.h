@@ -16,7 +16,7 @@ constexpr int kTcBM = 128;
 constexpr int kTcBN = 256;
 constexpr int kTcSlabBytes = 128;  // one K slab row = one 128-byte swizzle row
 constexpr int kTcStages = 6;
-constexpr int kTcThreads = 320;    // warp 0 TMA, warp 1 MMA + TMEM, warps 2-9 epilogue
+constexpr int kTcThreads = 384;    // warp 0 TMA, warp 1 MMA + TMEM, warps 2-3 idle, warps 4-11 epilogue
 constexpr int kTcPair = 2;         // CTAs per cluster running one cta_group::2 MMA
 
 // fp32 FFMA GEMM tile
@@ -84,6 +84,12 @@ struct GemmGroup {
     int32_t kseg;
     int32_t sym;            // symmetric D: lower-triangle tiles, mirrored stores
     int32_t tiles_m, tiles_n, tiles_per_mat;
+    // tcgen05 symmetric groups with m <= 128: matrices per 256 x 256 pair tile
+    // (2 for m <= 128, 4 for m <= 64), laid block-diagonally -- CTA rank r
+    // loads matrices mat + r pack/2 .. as its 128 rows of A and B, and block
+    // (i, i) of the accumulator is matrix mat + i's product; 1 otherwise
+    int32_t pack;
+    int32_t ntiles;         // tiles of the whole group: tiles_per_mat * batch, or batch / pack rounded up
     int32_t slot_base;      // slot of batch entry 0
     // epilogue: v = alpha * (c_acc*acc + c_diag*[r==c] + c_aux*aux[r][c])
     int32_t mode;           // EpiMode

@@ -80,6 +80,7 @@ struct dmuon_plan_s {
     int32_t scale_rule = DMUON_SCALE_ASPECT;
     int32_t nesterov = 1;
     int32_t small_m = 256;
+    int32_t tile_rule = DMUON_TILE_PACKED;
     uint64_t budget = 0;
 
     int64_t count = 0;
