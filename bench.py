@@ -44,7 +44,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-adamw", action="store_true", help="skip the AdamW comparison step")
     ap.add_argument("--routes", choices=["auto", "tuned"], default="auto",
-                    help="tuned: time Gram against direct per bucket first (autotune cache), plan with the faster")
+                    help="tuned: time each bucket's routes (Gram, direct) and tile rules (packed, single) "
+                         "first (autotune cache), plan with the fastest")
     ap.add_argument("--owners", type=int, default=8,
                     help="owner-model leg: ranks D the set is split over (0 = skip)")
     ap.add_argument("--e2e-steps", type=int, default=10)
@@ -333,10 +334,10 @@ def run_dmuon(args, cfg, world, rank, local):
     budget = int((args.budget_gb or cfg.budget_gb) * (1 << 30))
     shapes = [(r, c, dt) for r, c in cfg.shapes]
     if args.routes == "tuned":
-        from matrix_orthogonalising_optimizer_gb300.autotune import autotune_routes
-        routes, _ = autotune_routes([(r, c, cfg.dtype) for r, c in cfg.shapes], precision=cfg.precision,
-                                    ns_steps=cfg.ns_steps)
-        shapes = [s + (rt,) for s, rt in zip(shapes, routes)]
+        from matrix_orthogonalising_optimizer_gb300.autotune import autotune_buckets
+        choices, _ = autotune_buckets([(r, c, cfg.dtype) for r, c in cfg.shapes], precision=cfg.precision,
+                                      ns_steps=cfg.ns_steps)
+        shapes = [s + ch for s, ch in zip(shapes, choices)]
     muon = Muon(shapes, precision=cfg.precision, workspace_budget=budget).bind()
     ws, gs, ms = workloads.make_set(cfg, "cuda")
     torch.cuda.synchronize()

@@ -80,10 +80,12 @@ extern "C" {
                                    product hi*hi + hi*lo + lo*hi; the final product's Q
                                    as hi + lo */
 
-/* tile rules of the tensor-core symmetric products of buckets with m <= 128 */
-#define DMUON_TILE_PACKED 0   /* 2 (m <= 128) or 4 (m <= 64) matrices per 256 x 256 pair
+/* tile rules of the tensor-core symmetric products of bf16 buckets with m <= 128
+   (larger buckets, and FP32 precision, always run one matrix per tile: SINGLE) */
+#define DMUON_TILE_AUTO 0     /* a shape: the plan's rule; the plan: PACKED */
+#define DMUON_TILE_PACKED 1   /* 2 (m <= 128) or 4 (m <= 64) matrices per 256 x 256 pair
                                  tile, laid block-diagonally */
-#define DMUON_TILE_SINGLE 1   /* one matrix per pair tile */
+#define DMUON_TILE_SINGLE 2   /* one matrix per pair tile */
 
 /* update-scale rules */
 #define DMUON_SCALE_ASPECT 0 /* s = sqrt(max(1, rows/cols)) */
@@ -114,6 +116,9 @@ typedef struct {
     int32_t route;    /* this matrix's route rule: 0 (DMUON_ROUTE_AUTO) = the plan's
                          options->route; DMUON_ROUTE_GRAM or DMUON_ROUTE_DIRECT override it
                          (e.g. from a measured per-bucket choice) */
+    int32_t tile;     /* this matrix's tile rule: 0 (DMUON_TILE_AUTO) = the plan's
+                         options->tile_rule; DMUON_TILE_PACKED or _SINGLE override it */
+    int32_t reserved; /* 0 */
 } dmuon_shape_t;
 
 /* Zero-initialised options give the defaults noted on each field. */
@@ -127,7 +132,7 @@ typedef struct {
     int32_t small_m;        /* AUTO route and BF16 mode: Gram buckets with m <= small_m run
                                their m x m products on split-bf16 tensor cores
                                (DMUON_ENGINE_TC_SPLIT); 0 => 256; < 0 => none */
-    int32_t tile_rule;      /* DMUON_TILE_*; default PACKED */
+    int32_t tile_rule;      /* DMUON_TILE_*; 0 (AUTO) => PACKED */
     uint64_t workspace_budget; /* bytes for one wave of buckets; 0 => everything in one wave */
 } dmuon_options_t;
 
@@ -135,7 +140,7 @@ typedef struct {
     int32_t dtype;     /* DMUON_BF16 | DMUON_FP32 */
     int32_t route;     /* DMUON_BUCKET_GRAM | DMUON_BUCKET_DIRECT */
     int32_t mm_engine; /* DMUON_ENGINE_* used for the m x m products */
-    int32_t reserved;
+    int32_t tile;      /* DMUON_TILE_PACKED or DMUON_TILE_SINGLE (the bucket's resolved rule) */
     int64_t m, n;      /* canonical short and long side */
     int64_t count;     /* matrices in the bucket */
     int64_t per_matrix_bytes; /* workspace bytes one matrix of the bucket needs in a wave */
@@ -151,13 +156,16 @@ typedef struct {
  * (tall matrices are packed transposed), and its route resolved: the shape's
  * own rule, else options->route; AUTO gives Gram when n >= 3m or m <=
  * small_m, else direct; FP32 precision gives Gram unless the rule is DIRECT.
- * Buckets are keyed (dtype, m, n, route), ordered by that key ascending
+ * Its tile rule likewise: the shape's own, else options->tile_rule, AUTO
+ * meaning PACKED; SINGLE wherever packing does not apply (m > 128, FP32).
+ * Buckets are keyed (dtype, m, n, route, tile), ordered by that key ascending
  * (DMUON_BUCKET_GRAM before DMUON_BUCKET_DIRECT); matrices keep their input
  * order inside a bucket.  Buckets are then packed, in bucket order, into waves whose
  * workspace fits options->workspace_budget, splitting a bucket where needed.
  * Returns NULL on error (message in dmuon_last_error): count < 1, a NULL
  * pointer, a dimension outside [1, DMUON_MAX_DIM], rows*cols >=
- * DMUON_MAX_ELEMS, an unknown dtype, an unknown shape route, bad options,
+ * DMUON_MAX_ELEMS, an unknown dtype, an unknown shape route or tile rule, a
+ * nonzero reserved field, bad options,
  * or a budget smaller than one matrix. */
 dmuon_handle_t dmuon_plan(const dmuon_shape_t* shapes, int64_t count);
 dmuon_handle_t dmuon_plan_ex(const dmuon_shape_t* shapes, int64_t count,

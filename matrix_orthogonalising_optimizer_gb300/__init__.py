@@ -16,7 +16,7 @@ import ctypes
 from . import _lib
 from ._lib import (  # noqa: F401
     BF16, FP32, PREC_BF16, PREC_FP32, ROUTE_AUTO, ROUTE_GRAM, ROUTE_DIRECT, BUCKET_GRAM, BUCKET_DIRECT,
-    ENGINE_TC_BF16, ENGINE_SIMT_FP32, ENGINE_TC_SPLIT, TILE_PACKED, TILE_SINGLE, SCALE_ASPECT, SCALE_RMS, TIMER_NAMES, ASSIGN_GREEDY, ASSIGN_EXACT, DmuonError,
+    ENGINE_TC_BF16, ENGINE_SIMT_FP32, ENGINE_TC_SPLIT, TILE_AUTO, TILE_PACKED, TILE_SINGLE, SCALE_ASPECT, SCALE_RMS, TIMER_NAMES, ASSIGN_GREEDY, ASSIGN_EXACT, DmuonError,
 )
 
 __all__ = ["Muon", "dmuon_plan", "dmuon_step", "assign_owners", "adamw_step", "load"]
@@ -25,7 +25,7 @@ _DTYPES = {"bf16": BF16, "fp32": FP32}
 _PREC = {"bf16": PREC_BF16, "fp32": PREC_FP32}
 _ROUTES = {"auto": ROUTE_AUTO, "gram": ROUTE_GRAM, "direct": ROUTE_DIRECT}
 _SCALES = {"aspect": SCALE_ASPECT, "rms": SCALE_RMS}
-_TILES = {"packed": TILE_PACKED, "single": TILE_SINGLE}
+_TILES = {"auto": TILE_AUTO, "packed": TILE_PACKED, "single": TILE_SINGLE}
 
 
 def load():
@@ -42,9 +42,10 @@ def _stream_handle(stream):
 
 
 def dmuon_plan(shapes, dtype="bf16", precision="bf16", route="auto", coeffs=None, eps=0.0,
-               scale_rule="aspect", nesterov=True, small_m=0, workspace_budget=0, tile="packed"):
-    """dmuon_plan_ex: shapes is a list of (rows, cols[, dtype[, route]]); a shape's route
-    ("auto" / 0 = the plan's ``route``, "gram", "direct") overrides the plan's rule."""
+               scale_rule="aspect", nesterov=True, small_m=0, workspace_budget=0, tile="auto"):
+    """dmuon_plan_ex: shapes is a list of (rows, cols[, dtype[, route[, tile]]]); a shape's
+    route ("auto" / 0 = the plan's ``route``, "gram", "direct") and tile rule ("auto" / 0 =
+    the plan's ``tile``, "packed", "single") override the plan's rules."""
     lib = _lib.load()
     arr = (_lib.Shape * len(shapes))()
     for i, s in enumerate(shapes):
@@ -53,6 +54,8 @@ def dmuon_plan(shapes, dtype="bf16", precision="bf16", route="auto", coeffs=None
         arr[i].dtype = _DTYPES[dt] if isinstance(dt, str) else int(dt)
         rt = s[3] if len(s) > 3 else 0
         arr[i].route = _ROUTES[rt] if isinstance(rt, str) else int(rt)
+        tl = s[4] if len(s) > 4 else 0
+        arr[i].tile = _TILES[tl] if isinstance(tl, str) else int(tl)
     opt = _lib.Options()
     opt.precision = _PREC[precision]
     opt.route = _ROUTES[route]
@@ -158,7 +161,7 @@ class Muon:
             mem = (ctypes.c_int64 * info.count)()
             _lib.check(self.lib.dmuon_plan_bucket_members(self.handle, b, mem), "dmuon_plan_bucket_members")
             out.append({"dtype": info.dtype, "m": info.m, "n": info.n, "route": info.route,
-                        "engine": info.mm_engine, "per_matrix_bytes": info.per_matrix_bytes,
+                        "engine": info.mm_engine, "tile": info.tile, "per_matrix_bytes": info.per_matrix_bytes,
                         "members": list(mem)})
         return out
 

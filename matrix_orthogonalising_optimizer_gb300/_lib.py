@@ -14,7 +14,7 @@ PREC_BF16, PREC_FP32 = 0, 1
 ROUTE_AUTO, ROUTE_GRAM, ROUTE_DIRECT = 0, 1, 2
 BUCKET_GRAM, BUCKET_DIRECT = 1, 2
 ENGINE_TC_BF16, ENGINE_SIMT_FP32, ENGINE_TC_SPLIT = 0, 1, 2
-TILE_PACKED, TILE_SINGLE = 0, 1
+TILE_AUTO, TILE_PACKED, TILE_SINGLE = 0, 1, 2
 SCALE_ASPECT, SCALE_RMS = 0, 1
 OK = 0
 ERR_INVALID_ARG, ERR_ALIGN, ERR_NO_WORKSPACE, ERR_UNSUPPORTED_DTYPE = -1, -2, -3, -4
@@ -26,7 +26,8 @@ ASSIGN_GREEDY, ASSIGN_EXACT = 0, 1
 
 
 class Shape(ctypes.Structure):
-    _fields_ = [("rows", c_int64), ("cols", c_int64), ("dtype", c_int32), ("route", c_int32)]
+    _fields_ = [("rows", c_int64), ("cols", c_int64), ("dtype", c_int32), ("route", c_int32), ("tile", c_int32),
+                ("reserved", c_int32)]
 
 
 class Options(ctypes.Structure):
@@ -36,7 +37,7 @@ class Options(ctypes.Structure):
 
 
 class BucketInfo(ctypes.Structure):
-    _fields_ = [("dtype", c_int32), ("route", c_int32), ("mm_engine", c_int32), ("reserved", c_int32),
+    _fields_ = [("dtype", c_int32), ("route", c_int32), ("mm_engine", c_int32), ("tile", c_int32),
                 ("m", c_int64), ("n", c_int64), ("count", c_int64), ("per_matrix_bytes", c_int64)]
 
 

@@ -1,19 +1,22 @@
-"""Per-bucket route autotune with a cache (plan time, on the GPU that will run the steps).
+"""Per-bucket route and tile autotune with a cache (plan time, on the GPU that will run the steps).
 
 The DMuon pages choose work from measured costs rather than FLOP counts
-(technical summary, section 2.3) and tune their kernels per shape (section
-2.4).  Here the choice tuned is each bucket's Newton-Schulz form.  The AUTO
+(technical summary, section 2.3) and tune their kernels' tiles per shape
+(section 2.4).  Here the choices tuned are each bucket's Newton-Schulz form
+and, for bf16 buckets with m <= 128, its tile rule: several matrices packed
+block-diagonally into one 256 x 256 pair tile, or one matrix per tile.  The AUTO
 rule picks Gram space where the bf16 Gram recurrence is accurate enough (n >=
 3m, or small m with split-bf16 m x m products); the direct form is accurate
 for every shape with m >= 128, so where AUTO picks Gram both forms are
-candidates there, Gram alone below, and elsewhere direct is the only one.  Each candidate is timed as a step over a
-sample of matrices of the bucket's shape (seeded synthetic data, CUDA events
-on the stream), and the faster is kept.
+candidates there, Gram alone below, and elsewhere direct is the only one.
+Each (route, tile) candidate is timed as a step over a sample of matrices of
+the bucket's shape (seeded synthetic data, CUDA events on the stream), and
+the fastest is kept.
 
 Results are cached per (m, n, dtype, precision, ns_steps) in a dict that can
 be saved as JSON, so a set is timed once per machine.  The routes come back
-per shape, ready to pass as the fourth element of each shape to ``Muon`` /
-``dmuon_plan``.  The timing runs the library's own step; nothing here is on
+per shape, ready to pass as the fourth and fifth elements of each shape to
+``Muon`` / ``dmuon_plan``.  The timing runs the library's own step; nothing here is on
 the step's path.
 """
 from __future__ import annotations
@@ -24,7 +27,7 @@ import os
 from . import _lib
 from ._lib import BF16, FP32
 
-__all__ = ["candidates", "cache_key", "autotune_routes"]
+__all__ = ["candidates", "tile_candidates", "cache_key", "autotune_buckets"]
 
 _DT_NAMES = {BF16: "bf16", FP32: "fp32"}
 
@@ -49,6 +52,13 @@ def candidates(m: int, n: int, precision: str = "bf16", small_m: int = 0) -> lis
     return ["gram", "direct"] if m >= DIRECT_MIN_M else ["gram"]
 
 
+def tile_candidates(m: int, precision: str = "bf16") -> list:
+    """Tile rules a bucket may take: packing applies to the tensor-core
+    products of bf16 buckets with m <= 128; elsewhere the plan's (AUTO) rule,
+    which resolves to one matrix per tile."""
+    return ["packed", "single"] if precision == "bf16" and m <= 128 else ["auto"]
+
+
 def cache_key(m: int, n: int, dtype: str, precision: str, ns_steps: int) -> str:
     return f"{m}x{n}:{dtype}:{precision}:T{ns_steps}"
 
@@ -57,7 +67,7 @@ def _dtype_name(dt) -> str:
     return dt if isinstance(dt, str) else _DT_NAMES[int(dt)]
 
 
-def _time_route(m, n, dtype, precision, route, ns_steps, sample, steps, seed):
+def _time_choice(m, n, dtype, precision, route, tile, ns_steps, sample, steps, seed):
     import torch
 
     from . import Muon
@@ -66,7 +76,7 @@ def _time_route(m, n, dtype, precision, route, ns_steps, sample, steps, seed):
     w = [(torch.randn(m, n, device="cuda", generator=g) * 0.02).to(tdt) for _ in range(sample)]
     gr = [(torch.randn(m, n, device="cuda", generator=g) * 1e-3).to(tdt) for _ in range(sample)]
     mo = [torch.zeros(m, n, device="cuda", dtype=tdt) for _ in range(sample)]
-    opt = Muon([(m, n, dtype, route)] * sample, precision=precision).bind()
+    opt = Muon([(m, n, dtype, route, tile)] * sample, precision=precision).bind()
     stream = torch.cuda.current_stream()
     for _ in range(2):
         opt.step(w, gr, mo, 0.02, 0.95, 0.01, ns_steps, stream)
@@ -85,23 +95,23 @@ def _time_route(m, n, dtype, precision, route, ns_steps, sample, steps, seed):
     return ms
 
 
-def autotune_routes(shapes, precision: str = "bf16", ns_steps: int = 5, small_m: int = 0, cache=None,
-                    cache_path: str | None = None, sample: int = 8, steps: int = 3, timer=None):
-    """Route per shape ("gram" / "direct") and the cache table.
+def autotune_buckets(shapes, precision: str = "bf16", ns_steps: int = 5, small_m: int = 0, cache=None,
+                     cache_path: str | None = None, sample: int = 8, steps: int = 3, timer=None):
+    """(route, tile) per shape and the cache table.
 
     shapes: (rows, cols[, dtype]) as for ``Muon``.  cache: a dict from an
     earlier call (updated in place); cache_path: a JSON file read first and
-    written back.  Each untimed (m, n, dtype) with two candidates is timed
-    with ``sample`` matrices (at most the bucket's own count) over ``steps``
-    steps; ``timer`` replaces the GPU timing (tests).  One candidate: no
-    timing, the entry records the route alone.
+    written back.  Each untimed (m, n, dtype) with several candidates is
+    timed with ``sample`` matrices (at most the bucket's own count) over
+    ``steps`` steps; ``timer`` replaces the GPU timing (tests).  One
+    candidate: no timing, the entry records it alone.
     """
     if cache is None:
         cache = {}
     if cache_path and os.path.exists(cache_path):
         with open(cache_path) as f:
             cache.update(json.load(f))
-    timer = timer or _time_route
+    timer = timer or _time_choice
     counts = {}
     keys = []
     for s in shapes:
@@ -114,18 +124,23 @@ def autotune_routes(shapes, precision: str = "bf16", ns_steps: int = 5, small_m:
         key = cache_key(m, n, dtype, precision, ns_steps)
         if key in cache:
             continue
-        cand = candidates(m, n, precision, small_m)
+        cand = [f"{r}/{t}" for r in candidates(m, n, precision, small_m) for t in tile_candidates(m, precision)]
         entry = {"candidates": cand, "ms_per_matrix": {}}
         if len(cand) > 1:
             k = max(1, min(sample, count))
-            for i, route in enumerate(cand):
-                entry["ms_per_matrix"][route] = timer(m, n, dtype, precision, route, ns_steps, k, steps, 1000 + i)
-            entry["route"] = min(cand, key=lambda r: entry["ms_per_matrix"][r])
+            for i, c in enumerate(cand):
+                route, tile = c.split("/")
+                entry["ms_per_matrix"][c] = timer(m, n, dtype, precision, route, tile, ns_steps, k, steps, 1000 + i)
+            best = min(cand, key=lambda c: entry["ms_per_matrix"][c])
         else:
-            entry["route"] = cand[0]
+            best = cand[0]
+        entry["route"], entry["tile"] = best.split("/")
         cache[key] = entry
     if cache_path:
         with open(cache_path, "w") as f:
             json.dump(cache, f, indent=1, sort_keys=True)
-    routes = [cache[cache_key(m, n, dt, precision, ns_steps)]["route"] for m, n, dt in keys]
-    return routes, cache
+    out = []
+    for m, n, dt in keys:
+        e = cache[cache_key(m, n, dt, precision, ns_steps)]
+        out.append((e["route"], e["tile"]))
+    return out, cache

@@ -41,6 +41,28 @@ int64_t split_ld(int64_t m) { return 2 * static_cast<int64_t>(up(static_cast<uin
 
 bool split_operand(int k) { return k == BUF_RB || k == BUF_P || k == BUF_Q0 || k == BUF_Q1 || k == BUF_RP; }
 
+// The momentum pass streams a matrix flat when its packed u has the gradient's
+// own layout (bf16 storage and operands, not transposed, rows on 16 bytes)
+// and it is large enough for its record lookup to be amortised over many
+// chunks (2^20 elements); and only in waves where such matrices hold at
+// least kFlatWaveMin elements, since a second pass costs a launch and a tail.
+// Measured on the Llama-3-8B-shaped set: its wide matrices at 90 % of HBM
+// instead of 82 %; on sets of small matrices the extra pass was slower.
+constexpr int64_t kFlatMatrixMin = int64_t(1) << 20;
+constexpr int64_t kFlatWaveMin = int64_t(1) << 26;
+
+bool flat_momentum(int32_t precision, int32_t dtype, int64_t rows, int64_t cols) {
+    return precision == DMUON_PREC_BF16 && dtype == DMUON_BF16 && rows <= cols && cols % 8 == 0 &&
+           rows * cols >= kFlatMatrixMin;
+}
+
+// Momentum work units of a matrix: chunks of kMomChunk elements (flat) or
+// 64 x 64 tiles; either leaves kMomPartials sum-of-squares partials.
+int64_t momentum_units(bool flat, int64_t rows, int64_t cols) {
+    if (flat) return (rows * cols + kMomChunk - 1) / kMomChunk;
+    return ((rows + kMomTile - 1) / kMomTile) * ((cols + kMomTile - 1) / kMomTile);
+}
+
 // ------------------------------------------------------------ template kinds
 
 enum Tmpl : int {
@@ -151,7 +173,7 @@ struct GroupSpec {
     int64_t slot_base = 0;
 };
 
-int build_group(const GroupSpec& s, GemmGroup* g, int32_t tile_rule) {
+int build_group(const GroupSpec& s, GemmGroup* g, int32_t tile) {
     std::memset(g, 0, sizeof(*g));
     g->a = s.a.p;
     g->b = s.b.p;
@@ -199,7 +221,7 @@ int build_group(const GroupSpec& s, GemmGroup* g, int32_t tile_rule) {
             g->tiles_per_mat = g->tiles_m * g->tiles_n;
         }
         // small symmetric products: several matrices block-diagonally per tile
-        if (s.sym && tile_rule == DMUON_TILE_PACKED && s.M <= kTcBM) g->pack = s.M <= kTcBM / 2 ? 4 : 2;
+        if (s.sym && tile == DMUON_TILE_PACKED && s.M <= kTcBM) g->pack = s.M <= kTcBM / 2 ? 4 : 2;
         if (s.a.type != ELEM_BF16 || s.b.type != ELEM_BF16)
             return fail(DMUON_ERR_INVALID_ARG, "internal: tensor-core operands must be bf16");
         const int64_t ak = s.a_k ? s.a_k : s.K, bk = s.b_k ? s.b_k : s.K;
@@ -416,7 +438,7 @@ dmuon_handle_t dmuon_plan_ex(const dmuon_shape_t* shapes, int64_t count, const d
     }
     if (!(o.eps >= 0.0f) || !std::isfinite(o.eps) || !std::isfinite(o.ns_a) || !std::isfinite(o.ns_b) ||
         !std::isfinite(o.ns_c) || (o.no_nesterov != 0 && o.no_nesterov != 1) ||
-        (o.tile_rule != DMUON_TILE_PACKED && o.tile_rule != DMUON_TILE_SINGLE)) {
+        o.tile_rule < DMUON_TILE_AUTO || o.tile_rule > DMUON_TILE_SINGLE) {
         fail(DMUON_ERR_INVALID_ARG, "bad option values");
         return nullptr;
     }
@@ -432,7 +454,7 @@ dmuon_handle_t dmuon_plan_ex(const dmuon_shape_t* shapes, int64_t count, const d
     h->scale_rule = o.scale_rule;
     h->nesterov = o.no_nesterov ? 0 : 1;
     h->small_m = o.small_m == 0 ? 256 : o.small_m;
-    h->tile_rule = o.tile_rule;
+    h->tile_rule = o.tile_rule == DMUON_TILE_AUTO ? DMUON_TILE_PACKED : o.tile_rule;
     h->budget = o.workspace_budget;
     h->count = count;
     h->shapes.assign(shapes, shapes + count);
@@ -445,11 +467,18 @@ dmuon_handle_t dmuon_plan_ex(const dmuon_shape_t* shapes, int64_t count, const d
         if (rule == DMUON_ROUTE_DIRECT) return DMUON_BUCKET_DIRECT;
         return (n >= 3 * m || small) ? DMUON_BUCKET_GRAM : DMUON_BUCKET_DIRECT;
     };
-    std::map<std::tuple<int32_t, int64_t, int64_t, int32_t>, std::vector<int64_t>> keyed;
+    // tile rule of one matrix: its own, else the plan's; SINGLE where packing
+    // does not apply
+    auto resolve_tile = [&](int32_t own, int64_t m) {
+        if (h->precision == DMUON_PREC_FP32 || m > kTcBM) return static_cast<int32_t>(DMUON_TILE_SINGLE);
+        return own != DMUON_TILE_AUTO ? own : h->tile_rule;
+    };
+    std::map<std::tuple<int32_t, int64_t, int64_t, int32_t, int32_t>, std::vector<int64_t>> keyed;
     for (int64_t i = 0; i < count; ++i) {
         const dmuon_shape_t& s = shapes[i];
         if (s.rows < 1 || s.cols < 1 || s.rows > DMUON_MAX_DIM || s.cols > DMUON_MAX_DIM ||
-            s.rows * s.cols >= DMUON_MAX_ELEMS || s.route < DMUON_ROUTE_AUTO || s.route > DMUON_ROUTE_DIRECT) {
+            s.rows * s.cols >= DMUON_MAX_ELEMS || s.route < DMUON_ROUTE_AUTO || s.route > DMUON_ROUTE_DIRECT ||
+            s.tile < DMUON_TILE_AUTO || s.tile > DMUON_TILE_SINGLE || s.reserved != 0) {
             fail(DMUON_ERR_INVALID_ARG, "shape " + std::to_string(i) + " out of range");
             delete h;
             return nullptr;
@@ -461,7 +490,8 @@ dmuon_handle_t dmuon_plan_ex(const dmuon_shape_t* shapes, int64_t count, const d
         }
         const int64_t m = std::min(s.rows, s.cols), n = std::max(s.rows, s.cols);
         const int32_t rule = s.route != DMUON_ROUTE_AUTO ? s.route : h->route_rule;
-        keyed[std::make_tuple(s.dtype, m, n, static_cast<int32_t>(resolve(rule, m, n)))].push_back(i);
+        keyed[std::make_tuple(s.dtype, m, n, static_cast<int32_t>(resolve(rule, m, n)), resolve_tile(s.tile, m))]
+            .push_back(i);
     }
     int64_t slot = 0;
     for (auto& kv : keyed) {
@@ -472,6 +502,7 @@ dmuon_handle_t dmuon_plan_ex(const dmuon_shape_t* shapes, int64_t count, const d
         b.members = kv.second;
         const bool small = h->small_m > 0 && b.m <= h->small_m;
         b.route = std::get<3>(kv.first);
+        b.tile = std::get<4>(kv.first);
         if (h->precision == DMUON_PREC_FP32) b.engine = DMUON_ENGINE_SIMT_FP32;
         else if (b.route == DMUON_BUCKET_GRAM && small) b.engine = DMUON_ENGINE_TC_SPLIT;
         else b.engine = DMUON_ENGINE_TC_BF16;
@@ -532,7 +563,7 @@ dmuon_handle_t dmuon_plan_ex(const dmuon_shape_t* shapes, int64_t count, const d
     for (size_t wi = 0; wi < waves.size(); ++wi) {
         Wave w;
         uint64_t cur = 0;
-        int64_t tiles = 0;
+        int64_t tiles = 0, flat_elems = 0;
         for (size_t pi = 0; pi < waves[wi].size(); ++pi) {
             Piece p;
             std::tie(p.bucket, p.start, p.count) = waves[wi][pi];
@@ -548,7 +579,8 @@ dmuon_handle_t dmuon_plan_ex(const dmuon_shape_t* shapes, int64_t count, const d
                 sh.wave = static_cast<int64_t>(wi);
                 sh.piece = static_cast<int64_t>(pi);
                 sh.j = j;
-                tiles += ((sh.rows + 63) / 64) * static_cast<int64_t>((sh.cols + 63) / 64);
+                if (flat_momentum(h->precision, shapes[sh.gidx].dtype, sh.rows, sh.cols))
+                    flat_elems += static_cast<int64_t>(sh.rows) * sh.cols;
             }
             ngroups += b.route == DMUON_BUCKET_GRAM ? 9 : 10;
             w.pieces.push_back(p);
@@ -556,6 +588,12 @@ dmuon_handle_t dmuon_plan_ex(const dmuon_shape_t* shapes, int64_t count, const d
         w.slot0 = w.pieces.front().slot0;
         w.nslots = 0;
         for (const Piece& p : w.pieces) w.nslots += p.count;
+        w.flat = flat_elems >= kFlatWaveMin;
+        for (int64_t s = w.slot0; s < w.slot0 + w.nslots; ++s) {
+            const SlotHost& sh = h->slots[s];
+            const bool fl = w.flat && flat_momentum(h->precision, shapes[sh.gidx].dtype, sh.rows, sh.cols);
+            tiles += momentum_units(fl, sh.rows, sh.cols);
+        }
         w.bytes = cur;
         w.mom_tiles = tiles;
         max_wave = std::max(max_wave, cur);
@@ -569,7 +607,8 @@ dmuon_handle_t dmuon_plan_ex(const dmuon_shape_t* shapes, int64_t count, const d
     h->off_ptrs = h->off_infos + up(nslots * sizeof(MatInfo), 256);
     h->off_groups = h->off_ptrs + up(3 * static_cast<uint64_t>(count) * sizeof(void*), 256);
     h->off_counters = h->off_groups + up(static_cast<uint64_t>(ngroups) * sizeof(GemmGroup), 256);
-    h->off_waves = h->off_counters + up(kMaxLaunchesPerWave * sizeof(int32_t), 256);
+    h->off_flat = h->off_counters + up(kMaxLaunchesPerWave * sizeof(int32_t), 256);
+    h->off_waves = h->off_flat + up(nslots * sizeof(int32_t), 256);
     h->ws_bytes = h->off_waves + max_wave;
     return h;
 }
@@ -592,6 +631,7 @@ int dmuon_plan_bucket(dmuon_handle_t h, int64_t i, dmuon_bucket_info_t* out) {
     out->dtype = b.dtype;
     out->route = b.route;
     out->mm_engine = b.engine;
+    out->tile = b.tile;
     out->m = b.m;
     out->n = b.n;
     out->count = static_cast<int64_t>(b.members.size());
@@ -718,18 +758,29 @@ int dmuon_bind_workspace(dmuon_handle_t h, void* dev_ptr, size_t bytes) {
         mi.rows = sh.rows;
         mi.cols = sh.cols;
         mi.tiles_c = (sh.cols + 63) / 64;
-        mi.ntiles = ((sh.rows + 63) / 64) * mi.tiles_c;
+        mi.flat = h->waves[sh.wave].flat && flat_momentum(h->precision, h->shapes[sh.gidx].dtype, sh.rows, sh.cols);
+        mi.ntiles = static_cast<int32_t>(momentum_units(mi.flat != 0, sh.rows, sh.cols));
         mi.transposed = sh.transposed;
         mi.dtype = sh.dtype;
         mi.x_type = x.type;
         mi.scale = shape_scale(h->scale_rule, sh.rows, sh.cols);
     }
-    for (const Wave& w : h->waves) {
-        int64_t t = 0;
+    // per wave: the tile pass's index over all slots, the flat pass's over
+    // the flat slots (listed, wave-relative, in the flat table)
+    std::vector<int32_t> flat_list(h->slots.size());
+    for (Wave& w : h->waves) {
+        int64_t t = 0, f = 0;
+        w.nflat = 0;
         for (int64_t s = w.slot0; s < w.slot0 + w.nslots; ++s) {
             infos[s].tile_begin = t;
             t += infos[s].ntiles;
+            if (infos[s].flat) {
+                infos[s].flat_begin = f;
+                f += infos[s].ntiles;
+                flat_list[w.slot0 + w.nflat++] = static_cast<int32_t>(s - w.slot0);
+            }
         }
+        w.flat_chunks = f;
     }
 
     // launch templates
@@ -751,7 +802,7 @@ int dmuon_bind_workspace(dmuon_handle_t h, void* dev_ptr, size_t bytes) {
             auto add = [&](int kind, GroupSpec s) -> int {
                 s.batch = p.count;
                 s.slot_base = p.slot0;
-                const int rc2 = build_group(s, &h->groups[next], h->tile_rule);
+                const int rc2 = build_group(s, &h->groups[next], b.tile);
                 if (rc2) return rc2;
                 gk[next] = s.kernel;
                 p.tmpl[kind] = static_cast<int32_t>(next++);
@@ -931,6 +982,8 @@ int dmuon_bind_workspace(dmuon_handle_t h, void* dev_ptr, size_t bytes) {
     if (cudaMemset(ws, 0, h->off_infos) != cudaSuccess ||
         cudaMemcpy(ws + h->off_infos, infos.data(), infos.size() * sizeof(MatInfo), cudaMemcpyHostToDevice) !=
             cudaSuccess ||
+        cudaMemcpy(ws + h->off_flat, flat_list.data(), flat_list.size() * sizeof(int32_t), cudaMemcpyHostToDevice) !=
+            cudaSuccess ||
         cudaMemset(ws + h->off_ptrs, 0, 3 * static_cast<size_t>(h->count) * sizeof(void*)) != cudaSuccess ||
         cudaMemcpy(ws + h->off_groups, h->groups.data(), h->groups.size() * sizeof(GemmGroup),
                    cudaMemcpyHostToDevice) != cudaSuccess)
@@ -997,12 +1050,19 @@ int dmuon_step_ex(dmuon_handle_t h, void* const* params, const void* const* grad
         ma.scalars = reinterpret_cast<SlotScalars*>(h->ws + h->off_scalars) + w.slot0;
         ma.grads = reinterpret_cast<const void* const*>(dptr + n);
         ma.moms = dptr + 2 * n;
+        ma.flat_slots = reinterpret_cast<const int32_t*>(h->ws + h->off_flat) + w.slot0;
+        ma.status = reinterpret_cast<int32_t*>(h->ws + h->off_status);
         ma.nslots = static_cast<int32_t>(w.nslots);
+        ma.nflat = static_cast<int32_t>(w.nflat);
         ma.total_tiles = w.mom_tiles;
+        ma.flat_chunks = w.flat_chunks;
         ma.beta = beta;
         ma.nesterov = h->nesterov;
         ma.eps = h->eps;
-        cudaError_t e = timed(h, s, DMUON_TIMER_MOMENTUM, -1, [&] { return launch_momentum_pack(ma, s); });
+        cudaError_t e = timed(h, s, DMUON_TIMER_MOMENTUM, -1, [&] {
+            const cudaError_t r = launch_momentum_flat(ma, s);
+            return r != cudaSuccess ? r : launch_momentum_pack(ma, s);
+        });
         if (e == cudaSuccess) e = timed(h, s, DMUON_TIMER_NORM, -1, [&] { return launch_norm_finalize(ma, s); });
         if (e != cudaSuccess) return fail(DMUON_ERR_CUDA, std::string("momentum launch: ") + cudaGetErrorString(e));
         if (per_wave[wi].size() > static_cast<size_t>(kMaxLaunchesPerWave))

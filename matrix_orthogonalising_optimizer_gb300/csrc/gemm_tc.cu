@@ -181,6 +181,13 @@ __device__ __forceinline__ void st_cluster_u32(uint32_t addr, int32_t v) {
     asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
+// Arrive without release ordering on an mbarrier of this or the partner CTA:
+// for a signal that covers no memory operation of the arriving thread (an
+// accumulator whose every tcgen05.ld has already completed).
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
 // Arrive (release, cluster scope) on an mbarrier of this or the partner CTA.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
@@ -301,6 +308,21 @@ __device__ __forceinline__ int wait_tile(uint64_t* full, const int32_t* slots, i
 // After every thread of the reader has read slot k: give it back to the leader.
 __device__ __forceinline__ void release_tile(uint64_t* empty, int k) {
     mbar_arrive_cluster(mapa(saddr(&empty[k % kTileRing]), 0));
+}
+
+// The epilogue warps' form: every lane reads the slot with an acquire load,
+// which orders its later operations after the read, and __syncwarp orders all
+// lanes' reads before lane 0's arrive, so the arrive itself can be relaxed (a
+// release would wait for the warp's global stores of the previous tile to
+// drain at cluster scope).
+__device__ __forceinline__ int wait_tile_acquire(uint64_t* full, const int32_t* slots, int k, int32_t* status,
+                                                 int total) {
+    const int slot = k % kTileRing;
+    const uint32_t ph = static_cast<uint32_t>(k / kTileRing) & 1u;
+    if (!mbar_wait_cluster(&full[slot], ph, status)) return total;
+    int32_t t;
+    asm volatile("ld.acquire.cluster.shared::cta.b32 %0, [%1];" : "=r"(t) : "r"(saddr(&slots[slot])) : "memory");
+    return t;
 }
 
 // Static schedule over pair tiles: index -> (group, matrix, pair row, column
@@ -1060,9 +1082,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
         const int half = (warp - kEpiWarp0) / 4;  // which column part (of kColParts) of the 256 columns
         int it = 0;
         for (int k = 0;; ++k, ++it) {
-            const int t = wait_tile(S.tile_full, S.tile_slot, k, L.status, total);
+            const int t = wait_tile_acquire(S.tile_full, S.tile_slot, k, L.status, total);
             __syncwarp();
-            if (lane == 0) release_tile(S.tile_empty, k);
+            if (lane == 0) mbar_arrive_cluster_relaxed(mapa(saddr(&S.tile_empty[k % kTileRing]), 0));
             if (!named_bar_and(1 + half, t < total)) break;
             const TileCoord tc = decode_tile(L, t);
             const GemmGroup& g = L.groups[L.idx[tc.gi]];
@@ -1148,9 +1170,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
                 epi_finish<kSplit>(e, r, r0w, lane, c0, v, x, stg);
             }
             }
+            // Release the accumulator.  Each tcgen05.ld of it ended with
+            // tcgen05.wait::ld before its values were used, so every read of
+            // the TMEM columns is complete here; the arrive is relaxed: a
+            // release would also wait for this warp's global stores to drain
+            // at cluster scope (4-5 % of the step on short-K products), and
+            // nothing that reuses the accumulator reads them.
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(mapa(saddr(&S.acc_empty[buf]), 0));
+            if (lane == 0) mbar_arrive_cluster_relaxed(mapa(saddr(&S.acc_empty[buf]), 0));
         }
     }
 

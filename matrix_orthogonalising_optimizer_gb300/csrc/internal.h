@@ -28,6 +28,9 @@ constexpr int kSimtThreads = 256;
 constexpr int kMomTile = 64;
 constexpr int kMomThreads = 256;
 constexpr int kMomPartials = kMomThreads / 32;  // sum-of-squares partials per momentum tile (one per warp)
+// flat momentum pass: a chunk of a matrix stored row after row, as many
+// elements as a tile, streamed through shared memory by bulk copies
+constexpr int kMomChunk = kMomTile * kMomTile;
 
 constexpr int kMaxGroupsPerLaunch = 96;
 constexpr int kMaxLaunchesPerWave = 1024;  // tile counters in the workspace, cleared per wave
@@ -55,6 +58,12 @@ struct MatInfo {
     int32_t dtype;      // storage dtype of W, grad, momentum (ElemType)
     int32_t x_type;     // ElemType of the packed u
     float scale;        // update shape scale s
+    int32_t flat;       // bf16, not transposed, cols a multiple of 8: u has the
+                        // gradient's layout and the momentum pass streams the
+                        // matrix as chunks of kMomChunk elements (ntiles counts
+                        // chunks; tile_begin .. + ntiles is skipped by the tile pass)
+    int32_t pad;
+    int64_t flat_begin; // first chunk of this matrix among the wave's flat matrices
 };
 
 struct SlotScalars {
@@ -131,8 +140,12 @@ struct MomentumArgs {
     SlotScalars* scalars;    // same slots
     const void* const* grads;
     void* const* moms;
+    const int32_t* flat_slots;  // the wave's flat slots (relative to infos), ascending
+    int32_t* status;         // device status word (a bounded wait that gave up)
     int32_t nslots;
+    int32_t nflat;
     int64_t total_tiles;
+    int64_t flat_chunks;
     float beta;
     int32_t nesterov;
     float eps;
@@ -172,6 +185,7 @@ class PerDevice {
 // ---------------------------------------------------------------- launchers
 
 cudaError_t launch_momentum_pack(const MomentumArgs& a, cudaStream_t s);
+cudaError_t launch_momentum_flat(const MomentumArgs& a, cudaStream_t s);
 cudaError_t launch_norm_finalize(const MomentumArgs& a, cudaStream_t s);
 cudaError_t launch_gemm_tc(const LaunchList& l, int num_sms, cudaStream_t s);
 cudaError_t launch_gemm_simt(const LaunchList& l, cudaStream_t s);

@@ -10,7 +10,17 @@
 // sums a matrix's partials in a fixed order (so the result does not depend on
 // which other matrices share the launch) and writes inv = 1/(||u||_F + eps).
 //
-// HBM-bound.  Persistent blocks walk the tiles of every matrix of the wave,
+// HBM-bound.  Matrices whose u has the gradient's own layout (bf16, not
+// transposed, rows starting on 16 bytes) go through a flat pass: persistent
+// blocks stream chunks of kMomChunk elements of G and M into a six-stage
+// shared-memory ring with bulk asynchronous copies (cp.async.bulk, completion
+// counted on the stage's mbarrier) while the block's threads update the
+// current chunk from shared memory and store M' and u with 16-byte accesses;
+// a chunk leaves one sum-of-squares partial per warp, the tile pass's layout.
+// The other matrices go through the tile pass below, which jumps over the
+// flat matrices' index ranges.
+//
+// Tile pass.  Persistent blocks walk the tiles of every matrix of the wave,
 // keeping the current matrix's record and pointers in registers (a lookup
 // per tile would put a chain of dependent loads before every tile's data).
 // Each thread issues its 128-bit grad and momentum loads for both of its rows
@@ -97,7 +107,7 @@ __global__ void __launch_bounds__(kMomThreads, kMomMinBlocks) momentum_pack_kern
     void* mom = nullptr;
     int buf = 0;
     for (int64_t t = blockIdx.x; t < a.total_tiles; t += gridDim.x) {
-        if (t >= end) {
+        if (t >= end || t < begin) {
             // tiles are numbered matrix after matrix: search forward, trying
             // the next matrix first
             int lo = slot + 1, hi = a.nslots - 1;
@@ -111,6 +121,12 @@ __global__ void __launch_bounds__(kMomThreads, kMomMinBlocks) momentum_pack_kern
             const MatInfo& nm = a.infos[slot];
             begin = nm.tile_begin;
             end = begin + nm.ntiles;
+            if (nm.flat) {
+                // streamed by the flat pass: continue at this block's first
+                // index at or past the matrix's end
+                t += (end - t + gridDim.x - 1) / gridDim.x * gridDim.x - gridDim.x;
+                continue;
+            }
             grad = a.grads[nm.gidx];
             mom = a.moms[nm.gidx];
         }
@@ -225,6 +241,197 @@ __global__ void __launch_bounds__(kMomThreads, kMomMinBlocks) momentum_pack_kern
     }
 }
 
+// ---------------------------------------------------------------- flat pass
+
+constexpr int kFlatThreads = 256;
+constexpr int kFlatStages = 6;
+constexpr int kFlatPiece = kMomChunk * 2;  // 8 KB: one bf16 array's share of a chunk
+constexpr int kFlatBlocksPerSm = 2;
+constexpr uint64_t kWaitNs = 2000000000ull;  // bounded waits: about 2 s
+static_assert(kMomChunk == 2 * 8 * kFlatThreads, "a thread updates two 8-element vectors of a chunk");
+
+struct __align__(128) FlatSmem {
+    uint8_t piece[kFlatStages][2][kFlatPiece];  // grad, momentum
+    uint64_t full[kFlatStages];                 // both pieces landed (count 1 + bytes)
+    uint64_t empty[kFlatStages];                // every warp has read the stage
+};
+
+__device__ __forceinline__ uint32_t saddr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(saddr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the phase of the given parity; false (and DEV_TIMEOUT in
+// the status word) after about 2 s.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer() - t0 > kWaitNs) {
+            atomicExch(status, DEV_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
+
+// Position (in the flat list) of the flat slot holding chunk c of the wave's
+// flat index, at or after position `from`, whose matrix starts at or before
+// c: that one if the next matrix starts past c, else a binary search.
+__device__ __forceinline__ int find_flat(const MomentumArgs& a, int64_t c, int from) {
+    int lo = from, hi = a.nflat - 1;
+    if (lo < hi && a.infos[a.flat_slots[lo + 1]].flat_begin > c) return lo;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (a.infos[a.flat_slots[mid]].flat_begin <= c) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+// One thread's view of the flat matrix it is working in: the record is
+// re-read only when the chunk leaves the matrix.
+struct FlatCursor {
+    int pos = -1;  // position in the flat list (-1: none yet)
+    int64_t begin = 0, end = 0, elems = 0;
+    const __nv_bfloat16* grad = nullptr;
+    __nv_bfloat16* mom = nullptr;
+    __nv_bfloat16* x = nullptr;
+    float* partials = nullptr;
+
+    __device__ __forceinline__ void seek(const MomentumArgs& a, int64_t c) {
+        if (c >= begin && c < end) return;
+        // chunks come in increasing order: past this matrix, the next one on
+        pos = find_flat(a, c, c >= end ? pos + 1 : 0);
+        const MatInfo& mi = a.infos[a.flat_slots[pos]];
+        begin = mi.flat_begin;
+        end = begin + mi.ntiles;
+        elems = static_cast<int64_t>(mi.rows) * mi.cols;
+        grad = static_cast<const __nv_bfloat16*>(a.grads[mi.gidx]);
+        mom = static_cast<__nv_bfloat16*>(a.moms[mi.gidx]);
+        x = static_cast<__nv_bfloat16*>(mi.x);
+        partials = mi.partials;
+    }
+};
+
+// Thread 0: stream chunk c (if it is below c_end) into `stage`.  A chunk's
+// bytes are a multiple of 16 (the matrix's element count is a multiple of 8).
+__device__ __forceinline__ void flat_issue(const MomentumArgs& a, FlatSmem& S, FlatCursor& cur, int stage,
+                                           int64_t c, int64_t c_end) {
+    uint32_t bytes = 0;
+    int64_t e0 = 0;
+    if (c < c_end) {
+        cur.seek(a, c);
+        e0 = (c - cur.begin) * kMomChunk;
+        bytes = static_cast<uint32_t>(min(static_cast<int64_t>(kMomChunk), cur.elems - e0) * 2);
+    }
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(saddr(&S.full[stage])),
+                 "r"(2 * bytes)
+                 : "memory");
+    if (bytes == 0) return;
+    const void* src[2] = {cur.grad + e0, cur.mom + e0};
+#pragma unroll
+    for (int k = 0; k < 2; ++k)
+        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                         saddr(S.piece[stage][k])),
+                     "l"(reinterpret_cast<uint64_t>(src[k])), "r"(bytes), "r"(saddr(&S.full[stage]))
+                     : "memory");
+}
+
+__global__ void __launch_bounds__(kFlatThreads, kFlatBlocksPerSm) momentum_flat_kernel(
+    const __grid_constant__ MomentumArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    FlatSmem& S = *reinterpret_cast<FlatSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) {
+        for (int s = 0; s < kFlatStages; ++s) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(&S.full[s])), "r"(1) : "memory");
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(&S.empty[s])),
+                         "r"(kFlatThreads / 32)
+                         : "memory");
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    // a contiguous range of chunks per block: consecutive chunks mostly lie in
+    // one matrix, so its record is looked up once
+    const int64_t c_begin = a.flat_chunks * blockIdx.x / gridDim.x;
+    const int64_t c_end = a.flat_chunks * (blockIdx.x + 1) / gridDim.x;
+    FlatCursor issue_cur, cur;
+    if (tid == 0)
+        for (int s = 0; s < kFlatStages; ++s) flat_issue(a, S, issue_cur, s, c_begin + s, c_end);
+    bool ok = true;
+    int64_t it = 0;
+    for (int64_t c = c_begin; c < c_end; ++c, ++it) {
+        const int stage = static_cast<int>(it % kFlatStages);
+        const uint32_t phase = static_cast<uint32_t>(it / kFlatStages) & 1u;
+        if (!mbar_wait(&S.full[stage], phase, a.status)) {
+            ok = false;
+            break;
+        }
+        cur.seek(a, c);
+        const int64_t local = c - cur.begin, e0 = local * kMomChunk;
+        const int64_t nb = min(static_cast<int64_t>(kMomChunk), cur.elems - e0);
+        float ss = 0.0f;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int e = tid * 8 + h * (kMomChunk / 2);
+            if (e < nb) {
+                float g[8], m[8], u[8];
+                unpack8(*reinterpret_cast<const uint4*>(S.piece[stage][0] + 2 * e), g);
+                unpack8(*reinterpret_cast<const uint4*>(S.piece[stage][1] + 2 * e), m);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    m[k] = fmaf(a.beta, m[k], g[k]);
+                    u[k] = a.nesterov ? fmaf(a.beta, m[k], g[k]) : m[k];
+                    ss = fmaf(u[k], u[k], ss);
+                }
+                store8(cur.mom, e0 + e, ELEM_BF16, m);
+                store8(cur.x, e0 + e, ELEM_BF16, u);
+            }
+        }
+        // the warp's partial of this chunk (elements 256 w .. and 2048 + 256 w ..)
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss += __shfl_down_sync(0xffffffffu, ss, o);
+        if (lane == 0) cur.partials[local * kMomPartials + warp] = ss;
+        __syncwarp();
+        if (lane == 0)
+            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr(&S.empty[stage])) : "memory");
+        if (tid == 0) {
+            // every warp has read the stage: refill it
+            if (!mbar_wait(&S.empty[stage], phase, a.status)) {
+                ok = false;
+                break;
+            }
+            flat_issue(a, S, issue_cur, stage, c + kFlatStages, c_end);
+        }
+    }
+    if (tid == 0 && !ok) {
+        // let copies already issued land before the block exits
+        for (int s = 0; s < kFlatStages; ++s) {
+            const int64_t k = it + ((s - static_cast<int>(it % kFlatStages)) + kFlatStages) % kFlatStages;
+            mbar_wait(&S.full[s], static_cast<uint32_t>(k / kFlatStages) & 1u, a.status);
+        }
+    }
+}
+
 constexpr int kFinThreads = 256;
 
 __global__ void __launch_bounds__(kFinThreads) norm_finalize_kernel(const __grid_constant__ MomentumArgs a) {
@@ -279,6 +486,26 @@ cudaError_t launch_momentum_pack(const MomentumArgs& a, cudaStream_t s) {
     const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 1) * per_sm;
     const int grid = static_cast<int>(a.total_tiles < cap ? a.total_tiles : cap);
     momentum_pack_kernel<<<grid, kMomThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_momentum_flat(const MomentumArgs& a, cudaStream_t s) {
+    if (a.flat_chunks <= 0) return cudaSuccess;
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const size_t smem = sizeof(FlatSmem) + 128;
+    static PerDevice attr_per_device;
+    int unused = 0;
+    cudaError_t e = attr_per_device.get(dev, &unused, [&](int* out) {
+        *out = 1;
+        return cudaFuncSetAttribute(momentum_flat_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(smem));
+    });
+    if (e != cudaSuccess) return e;
+    const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 1) * kFlatBlocksPerSm;
+    const int grid = static_cast<int>(a.flat_chunks < cap ? a.flat_chunks : cap);
+    momentum_flat_kernel<<<grid, kFlatThreads, smem, s>>>(a);
     return cudaGetLastError();
 }
 

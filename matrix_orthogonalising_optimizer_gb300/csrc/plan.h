@@ -28,7 +28,7 @@ enum BufKind : int {
 };
 
 struct Bucket {
-    int32_t dtype = 0, route = 0, engine = 0;
+    int32_t dtype = 0, route = 0, engine = 0, tile = DMUON_TILE_SINGLE;
     int64_t m = 0, n = 0;
     std::vector<int64_t> members;  // input indices, input order
     int64_t pmb = 0;               // per-matrix workspace bytes
@@ -48,7 +48,10 @@ struct Wave {
     std::vector<Piece> pieces;
     int64_t slot0 = 0, nslots = 0;
     uint64_t bytes = 0;
-    int64_t mom_tiles = 0;
+    int64_t mom_tiles = 0;    // momentum units of all slots (tile pass index)
+    int64_t nflat = 0;        // flat slots (listed from the wave's slot0 in the flat table)
+    int64_t flat_chunks = 0;  // momentum units of the flat slots (flat pass index)
+    bool flat = false;        // the wave runs the flat momentum pass
 };
 
 struct Launch {
@@ -80,7 +83,7 @@ struct dmuon_plan_s {
     int32_t scale_rule = DMUON_SCALE_ASPECT;
     int32_t nesterov = 1;
     int32_t small_m = 256;
-    int32_t tile_rule = DMUON_TILE_PACKED;
+    int32_t tile_rule = DMUON_TILE_PACKED;  // the plan's rule (AUTO resolved)
     uint64_t budget = 0;
 
     int64_t count = 0;
@@ -91,7 +94,7 @@ struct dmuon_plan_s {
 
     // fixed region layout
     uint64_t off_status = 0, off_scalars = 0, off_infos = 0, off_ptrs = 0, off_groups = 0, off_counters = 0,
-             off_waves = 0;
+             off_flat = 0, off_waves = 0;
     int64_t num_groups = 0;
     uint64_t ws_bytes = 0;
 

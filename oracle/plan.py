@@ -13,7 +13,9 @@ C ABI header ``include/dmuon.h`` states for ``dmuon_plan``:
 * route per matrix: its own rule if the shape gives one, else the plan's;
   FP32 precision -> Gram unless the rule is DIRECT; AUTO -> Gram when
   n >= 3m or m <= small_m, else direct;
-* buckets keyed (dtype, m, n, route), ascending;
+* tile rule per matrix: its own if the shape gives one, else the plan's
+  (AUTO meaning PACKED); SINGLE where packing does not apply (m > 128, FP32);
+* buckets keyed (dtype, m, n, route, tile), ascending;
 * m x m engine: FP32 precision -> fp32 FFMA; BF16 precision -> split-bf16
   tensor cores for Gram buckets with m <= small_m, plain bf16 tensor cores
   otherwise;
@@ -32,6 +34,7 @@ PREC_BF16, PREC_FP32 = 0, 1
 ROUTE_AUTO, ROUTE_GRAM, ROUTE_DIRECT = 0, 1, 2
 BUCKET_GRAM, BUCKET_DIRECT = 1, 2
 ENGINE_TC_BF16, ENGINE_SIMT_FP32, ENGINE_TC_SPLIT = 0, 1, 2
+TILE_AUTO, TILE_PACKED, TILE_SINGLE = 0, 1, 2
 
 
 def _up(x: int, a: int) -> int:
@@ -62,12 +65,19 @@ def per_matrix_bytes(m: int, n: int, precision: int, route: int, engine: int) ->
 
 
 def plan_buckets(shapes, precision: int = PREC_BF16, route: int = ROUTE_AUTO,
-                 small_m: int = 0, budget: int = 0):
-    """shapes: list of (rows, cols, dtype[, route]).  Returns (buckets, waves).
+                 small_m: int = 0, budget: int = 0, tile: int = TILE_AUTO):
+    """shapes: list of (rows, cols, dtype[, route[, tile]]).  Returns (buckets, waves).
 
     buckets: list of dicts with dtype, m, n, members (input indices), route,
-    engine, per_matrix_bytes.  waves: list of lists of (bucket, start, count).
+    engine, tile, per_matrix_bytes.  waves: list of lists of (bucket, start, count).
     """
+    plan_tile = TILE_PACKED if tile == TILE_AUTO else tile
+
+    def resolve_tile(own, m):
+        if precision == PREC_FP32 or m > 128:
+            return TILE_SINGLE
+        return own if own != TILE_AUTO else plan_tile
+
     if small_m == 0:
         small_m = 256
     def resolve(rule, m, n):
@@ -83,11 +93,13 @@ def plan_buckets(shapes, precision: int = PREC_BF16, route: int = ROUTE_AUTO,
     for idx, shp in enumerate(shapes):
         rows, cols, dtype = shp[:3]
         own = shp[3] if len(shp) > 3 else ROUTE_AUTO
+        own_tile = shp[4] if len(shp) > 4 else TILE_AUTO
         m, n = min(rows, cols), max(rows, cols)
-        keyed.setdefault((dtype, m, n, resolve(own if own != ROUTE_AUTO else route, m, n)), []).append(idx)
+        key = (dtype, m, n, resolve(own if own != ROUTE_AUTO else route, m, n), resolve_tile(own_tile, m))
+        keyed.setdefault(key, []).append(idx)
     buckets = []
     for key in sorted(keyed):
-        dtype, m, n, r = key
+        dtype, m, n, r, t = key
         if precision == PREC_FP32:
             eng = ENGINE_SIMT_FP32
         elif r == BUCKET_GRAM and small_m > 0 and m <= small_m:
@@ -95,7 +107,7 @@ def plan_buckets(shapes, precision: int = PREC_BF16, route: int = ROUTE_AUTO,
         else:
             eng = ENGINE_TC_BF16
         buckets.append({"dtype": dtype, "m": m, "n": n, "members": keyed[key], "route": r,
-                        "engine": eng, "per_matrix_bytes": per_matrix_bytes(m, n, precision, r, eng)})
+                        "engine": eng, "tile": t, "per_matrix_bytes": per_matrix_bytes(m, n, precision, r, eng)})
     waves = []
     if budget == 0:
         waves.append([(b, 0, len(bk["members"])) for b, bk in enumerate(buckets)])

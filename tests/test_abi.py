@@ -33,16 +33,17 @@ def _lib_plan(shapes, **kw):
     return m, m.buckets(), m.waves()
 
 
-def _check_same(shapes, precision="bf16", route="auto", small_m=0, budget=0):
+def _check_same(shapes, precision="bf16", route="auto", small_m=0, budget=0, tile="auto"):
     pmap = {"bf16": oplan.PREC_BF16, "fp32": oplan.PREC_FP32}
     rmap = {"auto": oplan.ROUTE_AUTO, "gram": oplan.ROUTE_GRAM, "direct": oplan.ROUTE_DIRECT}
+    tmap = {"auto": oplan.TILE_AUTO, "packed": oplan.TILE_PACKED, "single": oplan.TILE_SINGLE}
     want_b, want_w = oplan.plan_buckets(shapes, precision=pmap[precision], route=rmap[route], small_m=small_m,
-                                        budget=budget)
+                                        budget=budget, tile=tmap[tile])
     _, got_b, got_w = _lib_plan(shapes, precision=precision, route=route, small_m=small_m,
-                                workspace_budget=budget)
+                                workspace_budget=budget, tile=tile)
     assert len(got_b) == len(want_b)
     for g, w in zip(got_b, want_b):
-        for k in ("dtype", "m", "n", "members", "route", "engine", "per_matrix_bytes"):
+        for k in ("dtype", "m", "n", "members", "route", "engine", "tile", "per_matrix_bytes"):
             assert g[k] == w[k], (k, g, w)
     assert got_w == [list(x) for x in want_w]
 
@@ -94,6 +95,28 @@ def test_planner_per_shape_routes_match_oracle(seed):
         assert got == want
 
 
+@pytest.mark.parametrize("seed", range(3))
+def test_planner_per_shape_tiles_match_oracle(seed):
+    # a shape's own tile rule overrides the plan's; it splits buckets only where
+    # packing applies (bf16, m <= 128)
+    g = torch.Generator().manual_seed(200 + seed)
+    base = [(r, c, 0) for r, c in workloads.random_shapes(seed, 90, 1, 300)]
+    base = base + base[:40]
+    shapes = [s + (int(torch.randint(0, 3, (1,), generator=g)), int(torch.randint(0, 3, (1,), generator=g)))
+              for s in base]
+    for prec in ("bf16", "fp32"):
+        for tile in ("auto", "packed", "single"):
+            _check_same(shapes, precision=prec, tile=tile)
+    _, got, _ = _lib_plan(shapes)
+    assert {b["tile"] for b in got if b["m"] > 128} <= {oplan.TILE_SINGLE}
+    assert {b["tile"] for b in got if b["m"] <= 128} == {oplan.TILE_PACKED, oplan.TILE_SINGLE}
+    # forcing a tile rule per shape equals forcing it for the plan
+    for t, name in ((1, "packed"), (2, "single")):
+        _, got, _ = _lib_plan([s[:3] + (0, t) for s in base])
+        _, want, _ = _lib_plan(base, tile=name)
+        assert got == want
+
+
 def test_planner_is_order_independent_up_to_members():
     shapes = [(r, c, 0) for r, c in workloads.random_shapes(3, 80, 1, 300)]
     perm = list(reversed(range(len(shapes))))
@@ -105,9 +128,10 @@ def test_planner_is_order_independent_up_to_members():
 
 
 def test_plan_errors(lib):
-    def plan(rows, cols, dtype=0, shape_route=0, **kw):
+    def plan(rows, cols, dtype=0, shape_route=0, shape_tile=0, shape_reserved=0, **kw):
         arr = (_lib.Shape * 1)()
         arr[0].rows, arr[0].cols, arr[0].dtype, arr[0].route = rows, cols, dtype, shape_route
+        arr[0].tile, arr[0].reserved = shape_tile, shape_reserved
         opt = _lib.Options()
         for k, v in kw.items():
             setattr(opt, k, v)
@@ -118,7 +142,9 @@ def test_plan_errors(lib):
                 dict(rows=1 << 20, cols=1 << 20), dict(rows=4, cols=4, dtype=7), dict(rows=4, cols=4, shape_route=3),
                 dict(rows=4, cols=4, shape_route=-1),
                 dict(rows=4, cols=4, precision=9), dict(rows=4, cols=4, route=5), dict(rows=4, cols=4, eps=-1.0),
-                dict(rows=4, cols=4, scale_rule=3), dict(rows=4, cols=4, no_nesterov=2)]:
+                dict(rows=4, cols=4, scale_rule=3), dict(rows=4, cols=4, no_nesterov=2),
+                dict(rows=4, cols=4, shape_tile=3), dict(rows=4, cols=4, shape_tile=-1),
+                dict(rows=4, cols=4, shape_reserved=1), dict(rows=4, cols=4, tile_rule=3)]:
         assert not plan(**bad), bad
         assert lib.dmuon_last_error()
     assert not lib.dmuon_plan(None, 1)

@@ -152,6 +152,30 @@ def test_momentum_many_one_tile_matrices():
     assert max(errs) <= TOL["bf16"], max(errs)
 
 
+@pytest.mark.gpu
+def test_flat_momentum_pass():
+    # A wave whose wide bf16 matrices of at least 2^20 elements hold 2^26 or
+    # more elements streams them through the flat (bulk-copy) momentum pass;
+    # a 1000 x 1056 matrix ends in a partial chunk.  Alone, the same matrices
+    # take the tile pass.  M' is the same element-wise formula either way
+    # (bitwise equal, within one ulp of the oracle); O meets the bf16 bar.
+    shapes = [(1024, 4096)] * 16 + [(1000, 1056)] * 2 + [(4096, 1024), (100, 300)]
+    inputs = make_inputs(shapes, "bf16", 41)
+    w_all, m_all, _ = run_step(shapes, inputs, "bf16", lr=1.0, beta=BETA, wd=0.0, zero_w=True)
+    picks = [0, 16, 17, 18, 19]
+    for i in picks:
+        w_one, m_one, _ = run_step([shapes[i]], [inputs[i]], "bf16", lr=1.0, beta=BETA, wd=0.0, zero_w=True)
+        assert torch.equal(m_one[0], m_all[i])
+        w, g, m = inputs[i]
+        want_m = oracle.round_to_storage(BETA * m.double().numpy() + g.double().numpy(), "bf16")
+        assert ulp_diff(m_all[i], torch.from_numpy(want_m).to(torch.bfloat16)).max() <= 1
+    want = oracle_O([inputs[i] for i in picks], beta=BETA)
+    for i, o in zip(picks, want):
+        r, c = shapes[i]
+        got = -w_all[i].double().numpy() / oracle.shape_scale(r, c)
+        assert rel_fro(got, o) <= TOL["bf16"], shapes[i]
+
+
 def test_zero_gradient_gives_pure_decay():
     shapes = [(320, 704), (48, 200), (300, 300)]
     inputs = [(w, torch.zeros_like(g), torch.zeros_like(m)) for w, g, m in make_inputs(shapes, "bf16", 17)]
