@@ -263,10 +263,12 @@ const char* dmuon_status_string(int status);
 /* ---- inspection (tests) ------------------------------------------------ */
 
 #define DMUON_BUF_X 0  /* packed u (and direct-route iterate 0) */
-#define DMUON_BUF_RF 1 /* Gram route: fp32 R after the last update; direct: fp32 A.  With the
-                          tensor-core m x m engine only its lower triangle is written (it is read
-                          only as the next polynomial's aux term). */
-#define DMUON_BUF_R_OPERAND 2 /* the operand copy of the same R / A that the products read
+#define DMUON_BUF_RF 1 /* Gram route: fp32 R after the last update; direct: fp32 A.  Held by
+                          the fp32 FFMA engine and the split engine (there only its lower
+                          triangle is written: it is read only as the next polynomial's b R
+                          term); the plain bf16 tensor-core engine has none (the b R term reads
+                          the bf16 operand) and the query fails for its buckets. */
+#define DMUON_BUF_R_OPERAND 2 /* the operand copy of R / A that the products read
                                  (bf16 on tensor cores, the fp32 buffer otherwise): both
                                  triangles, bitwise symmetric.  With DMUON_ENGINE_TC_SPLIT
                                  each row is [hi | lo], each part ld / 2 elements: hi =

@@ -87,7 +87,8 @@ void bucket_buffers(Bucket& b, int32_t precision) {
     set(BUF_X0, m * ldn, xt);
     if (b.route == DMUON_BUCKET_GRAM) {
         if (b.engine == DMUON_ENGINE_TC_BF16) {
-            set(BUF_RF, m * ldm, ELEM_F32);
+            // bf16 operands only: the polynomial's b R term reads the bf16 R
+            // the products read
             for (int k : {BUF_RB, BUF_P, BUF_Q0, BUF_Q1, BUF_RP}) set(k, m * ldm, ELEM_BF16);
         } else if (b.engine == DMUON_ENGINE_TC_SPLIT) {
             // fp32 R (aux of P); split operands [hi | lo], each part a whole
@@ -100,11 +101,11 @@ void bucket_buffers(Bucket& b, int32_t precision) {
         }
     } else {
         set(BUF_X1, m * ldn, xt);
-        set(BUF_RF, m * ldm, ELEM_F32);
-        if (precision == DMUON_PREC_BF16) {
+        if (precision == DMUON_PREC_BF16) {  // bf16 A only: B's b A term reads it too
             set(BUF_AB, m * ldm, ELEM_BF16);
             set(BUF_BB, m * ldm, ELEM_BF16);
         } else {
+            set(BUF_RF, m * ldm, ELEM_F32);
             set(BUF_BB, m * ldm, ELEM_F32);
         }
     }
@@ -844,10 +845,12 @@ int dmuon_bind_workspace(dmuon_handle_t h, void* dev_ptr, size_t bytes) {
                     s.K = n;
                     s.sym = true;
                     s.alpha = ALPHA_INV2;
-                    s.out[0] = RF;
-                    if (eng == kKernelTc) {
-                        s.out[1] = RB;
+                    if (split) {
+                        s.out[0] = RF;
                         s.out_lower_only[0] = true;  // fp32 R: only the next P's aux, lower triangle
+                        s.out[1] = RB;
+                    } else {
+                        s.out[0] = eng == kKernelTc ? RB : RF;
                     }
                     split_outputs(s);
                     if ((rc = add(G_SYRK, s))) return rc;
@@ -857,8 +860,11 @@ int dmuon_bind_workspace(dmuon_handle_t h, void* dev_ptr, size_t bytes) {
                     s.c_acc = h->ns_c;
                     s.c_diag = h->ns_a;
                     s.c_aux = h->ns_b;
-                    s.aux = RF;
-                    s.aux_sym = eng != kKernelTc;  // lower triangle only: read R[r][c], r >= c
+                    // the b R term: fp32 R (FFMA engine: read transposed, coalesced;
+                    // split engine: its lower triangle, read R[r][c], r >= c), or
+                    // the bf16 R the products read (plain tensor-core engine)
+                    s.aux = (eng == kKernelTc && !split) ? RB : RF;
+                    s.aux_sym = eng != kKernelTc;
                     s.out[0] = P;
                     if (first) {
                         s.out[1] = Q0;
@@ -882,10 +888,12 @@ int dmuon_bind_workspace(dmuon_handle_t h, void* dev_ptr, size_t bytes) {
                 }
                 {  // R <- P (R P)
                     GroupSpec s = sym_spec(eng, P, RP);
-                    s.out[0] = RF;
-                    if (eng == kKernelTc) {
-                        s.out[1] = RB;
+                    if (split) {
+                        s.out[0] = RF;
                         s.out_lower_only[0] = true;
+                        s.out[1] = RB;
+                    } else {
+                        s.out[0] = eng == kKernelTc ? RB : RF;
                     }
                     split_outputs(s);
                     if ((rc = add(G_RUPD, s))) return rc;
@@ -925,18 +933,14 @@ int dmuon_bind_workspace(dmuon_handle_t h, void* dev_ptr, size_t bytes) {
                     s.K = n;
                     s.sym = true;
                     s.alpha = sk.alpha;
-                    s.out[0] = AF;
-                    if (eng == kKernelTc) {
-                        s.out[1] = AB;
-                        s.out_lower_only[0] = true;  // fp32 A: only B's aux, lower triangle
-                    }
+                    s.out[0] = eng == kKernelTc ? AB : AF;
                     if ((rc = add(sk.kind, s))) return rc;
                 }
                 {  // B = bA + cA^2
                     GroupSpec s = sym_spec(eng, Aop, Aop);
                     s.c_acc = h->ns_c;
                     s.c_aux = h->ns_b;
-                    s.aux = AF;
+                    s.aux = eng == kKernelTc ? AB : AF;  // B's b A term: the A the product reads
                     s.aux_sym = eng != kKernelTc;
                     s.out[0] = BB;
                     if ((rc = add(D_A2, s))) return rc;

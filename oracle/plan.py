@@ -47,7 +47,7 @@ def per_matrix_bytes(m: int, n: int, precision: int, route: int, engine: int) ->
     bufs = [m * ldn * ex]                       # packed u
     if route == BUCKET_GRAM:
         if engine == ENGINE_TC_BF16:
-            bufs += [m * ldm * 4] + [m * ldm * 2] * 5      # Rf; Rb, P, Q0, Q1, RP
+            bufs += [m * ldm * 2] * 5                      # R, P, Q0, Q1, RP (bf16)
         elif engine == ENGINE_TC_SPLIT:
             # Rf; R, P, Q0, Q1, RP as bf16 rows [hi | lo], each part m rounded up to 64
             bufs += [m * ldm * 4] + [m * 2 * _up(m, 64) * 2] * 5
@@ -57,7 +57,7 @@ def per_matrix_bytes(m: int, n: int, precision: int, route: int, engine: int) ->
                 bufs += [m * ldm * 2]                      # bf16 Q for the final product
     else:
         if precision == PREC_BF16:
-            bufs += [m * ldn * 2, m * ldm * 4, m * ldm * 2, m * ldm * 2]  # X1; Af, Ab, B
+            bufs += [m * ldn * 2, m * ldm * 2, m * ldm * 2]              # X1; A, B (bf16)
         else:
             bufs += [m * ldn * 4, m * ldm * 4, m * ldm * 4]              # X1; A, B
     bufs += [4 * 8 * ((m + 63) // 64) * ((n + 63) // 64)]  # sum-of-squares partials: 8 per 64 x 64 tile

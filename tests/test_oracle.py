@@ -320,12 +320,14 @@ def test_plan_small_transformer_buckets():
 
 def test_plan_per_matrix_bytes_hand_worked():
     # m=3, n=5 Gram bucket on tensor cores: ldm = ldn = 8
-    # u: 3*8*2=48 -> 256; Rf: 3*8*4=96 -> 256; five bf16 m x m: 48 -> 256 each;
+    # u: 3*8*2=48 -> 256; five bf16 m x m: 48 -> 256 each;
     # partials (8 per tile, one tile) 32 -> 256
-    assert oplan.per_matrix_bytes(3, 5, oplan.PREC_BF16, oplan.BUCKET_GRAM, oplan.ENGINE_TC_BF16) == 8 * 256
+    assert oplan.per_matrix_bytes(3, 5, oplan.PREC_BF16, oplan.BUCKET_GRAM, oplan.ENGINE_TC_BF16) == 7 * 256
+    # direct bucket, bf16: u, X1, A, B -> 4 * 256, partials 256
+    assert oplan.per_matrix_bytes(3, 5, oplan.PREC_BF16, oplan.BUCKET_DIRECT, oplan.ENGINE_TC_BF16) == 5 * 256
     # 1024 x 4096 bf16 Gram, tensor cores
     m, n = 1024, 4096
-    want = m * n * 2 + m * m * 4 + 5 * m * m * 2 + 4 * 8 * 16 * 64
+    want = m * n * 2 + 5 * m * m * 2 + 4 * 8 * 16 * 64
     assert oplan.per_matrix_bytes(m, n, oplan.PREC_BF16, oplan.BUCKET_GRAM, oplan.ENGINE_TC_BF16) == want
 
 
