@@ -66,7 +66,7 @@ int64_t momentum_units(bool flat, int64_t rows, int64_t cols) {
 // ------------------------------------------------------------ template kinds
 
 enum Tmpl : int {
-    G_SYRK = 0, G_POLY0, G_POLY, G_Q01, G_Q10, G_RP, G_RUPD, G_FIN0, G_FIN1,
+    G_SYRK = 0, G_POLY0, G_POLY, G_Q01, G_Q10, G_RP0, G_RP, G_RUPD0, G_RUPD, G_FIN0, G_FIN1,
     D_SYRK0, D_SYRK_X0, D_SYRK_X1, D_A2, D_XUPD0, D_XUPD01, D_XUPD10, D_FIN0I, D_FIN0, D_FIN1,
     TMPL_COUNT
 };
@@ -297,9 +297,9 @@ std::vector<std::vector<int>> gram_sequence(int T) {
         seq.push_back({k == 0 ? G_POLY0 : G_POLY});
         std::vector<int> mid;
         if (k >= 1) mid.push_back((k - 1) % 2 == 0 ? G_Q01 : G_Q10);
-        if (k < T - 1) mid.push_back(G_RP);
+        if (k < T - 1) mid.push_back(k == 0 ? G_RP0 : G_RP);
         if (!mid.empty()) seq.push_back(mid);
-        if (k < T - 1) seq.push_back({G_RUPD});
+        if (k < T - 1) seq.push_back({k == 0 ? G_RUPD0 : G_RUPD});
     }
     seq.push_back({(T - 1) % 2 == 0 ? G_FIN0 : G_FIN1});
     return seq;
@@ -583,7 +583,7 @@ dmuon_handle_t dmuon_plan_ex(const dmuon_shape_t* shapes, int64_t count, const d
                 if (flat_momentum(h->precision, shapes[sh.gidx].dtype, sh.rows, sh.cols))
                     flat_elems += static_cast<int64_t>(sh.rows) * sh.cols;
             }
-            ngroups += b.route == DMUON_BUCKET_GRAM ? 9 : 10;
+            ngroups += b.route == DMUON_BUCKET_GRAM ? 11 : 10;
             w.pieces.push_back(p);
         }
         w.slot0 = w.pieces.front().slot0;
@@ -865,11 +865,10 @@ int dmuon_bind_workspace(dmuon_handle_t h, void* dev_ptr, size_t bytes) {
                     // the bf16 R the products read (plain tensor-core engine)
                     s.aux = (eng == kKernelTc && !split) ? RB : RF;
                     s.aux_sym = eng != kKernelTc;
-                    s.out[0] = P;
-                    if (first) {
-                        s.out[1] = Q0;
-                        if (QB.p) s.out[2] = QB;
-                    }
+                    // P0 is also Q0: it is stored once, in Q0, where step 0's R P and
+                    // R update read it
+                    s.out[0] = first ? Q0 : P;
+                    if (first && QB.p) s.out[1] = QB;
                     split_outputs(s);
                     if ((rc = add(first ? G_POLY0 : G_POLY, s))) return rc;
                 }
@@ -880,14 +879,14 @@ int dmuon_bind_workspace(dmuon_handle_t h, void* dev_ptr, size_t bytes) {
                     split_outputs(s);
                     if ((rc = add(dir == 0 ? G_Q01 : G_Q10, s))) return rc;
                 }
-                {  // R P
-                    GroupSpec s = sym_spec(eng, Rop, P);
+                for (int first = 1; first >= 0; --first) {  // R P (step 0: P0 held in Q0)
+                    GroupSpec s = sym_spec(eng, Rop, first ? Q0 : P);
                     s.out[0] = RP;
                     split_outputs(s);
-                    if ((rc = add(G_RP, s))) return rc;
+                    if ((rc = add(first ? G_RP0 : G_RP, s))) return rc;
                 }
-                {  // R <- P (R P)
-                    GroupSpec s = sym_spec(eng, P, RP);
+                for (int first = 1; first >= 0; --first) {  // R <- P (R P)
+                    GroupSpec s = sym_spec(eng, first ? Q0 : P, RP);
                     if (split) {
                         s.out[0] = RF;
                         s.out_lower_only[0] = true;
@@ -896,7 +895,7 @@ int dmuon_bind_workspace(dmuon_handle_t h, void* dev_ptr, size_t bytes) {
                         s.out[0] = eng == kKernelTc ? RB : RF;
                     }
                     split_outputs(s);
-                    if ((rc = add(G_RUPD, s))) return rc;
+                    if ((rc = add(first ? G_RUPD0 : G_RUPD, s))) return rc;
                 }
                 for (int qb = 0; qb < 2; ++qb) {  // W update from inv * Q X
                     GroupSpec s;
