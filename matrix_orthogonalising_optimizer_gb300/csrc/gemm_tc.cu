@@ -32,7 +32,11 @@
 //               leader so the next tile's MMAs overlap this tile's epilogue.
 // Operands use the 128-byte swizzle.  A is K-major (row-major M x K).  B is
 // K-major (stored N x K: symmetric operands and the Gram product) or MN-major
-// (stored K x N: the m x n iterate multiplied from the left).
+// (stored K x N: the m x n iterate multiplied from the left).  A group may
+// split K into parts (split-bf16 operands [hi | lo], see GemmGroup::kseg) and
+// store its bf16 outputs split (the kernel instance with kSplit = true); a
+// symmetric group of matrices with m <= 128 packs 2 or 4 of them
+// block-diagonally into one pair tile (GemmGroup::pack).
 //
 // Every mbarrier wait is bounded (about 2 s of %globaltimer); on expiry the
 // waiting thread records DEV_TIMEOUT in the status word and leaves its loop,
@@ -40,7 +44,8 @@
 // per-stage ring waits (full, empty) only order the async proxy's copies and
 // MMAs, which their mbarrier transactions already cover, and use CTA scope; a
 // cluster-scope acquire on them cost about 10 % of the step.  The tile ring
-// and the accumulator hand-off between the CTAs' threads use cluster scope.
+// and the accumulator hand-off between the CTAs' threads use cluster scope;
+// the epilogue warps' arrivals on them are relaxed (see their call sites).
 #include <cuda_bf16.h>
 
 #include "epilogue.cuh"
