@@ -372,6 +372,7 @@ static const std::vector<std::vector<Launch>>& launches_for(dmuon_plan_s* h, int
                     }
                     l.begin[l.n] = static_cast<int32_t>(tiles);
                     l.total_tiles = static_cast<int32_t>(tiles);
+                    l.update = l.n > 0 && h->groups[l.idx[0]].mode == EPI_UPDATE ? 1 : 0;
                     // the tcgen05 kernel's shared stage serves the transposed
                     // update or diagonal store chunks: never both in one launch
                     for (int j = 1; j < l.n; ++j)

@@ -131,6 +131,8 @@ struct LaunchList {
     int32_t n;                               // groups in this launch
     int32_t total_tiles;
     int32_t has_split;                       // some group stores split outputs (tcgen05 kernel instance)
+    int32_t epi_sets;                        // tcgen05 epilogue: alternate tiles per warp set (set at launch)
+    int32_t update;                          // the launch's products apply the W update (else they store)
     int32_t idx[kMaxGroupsPerLaunch];        // indices into `groups`
     int32_t begin[kMaxGroupsPerLaunch + 1];  // tile prefix
 };
