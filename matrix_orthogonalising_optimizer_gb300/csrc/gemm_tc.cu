@@ -101,9 +101,9 @@ struct __align__(1024) Smem {
     uint64_t tile_empty[kTileRing];  // leader only: every reader of both CTAs is done
     int32_t tile_slot[kTileRing];
     uint32_t tmem_base;
-    // transposed W update: a 16 x 128 chunk of v per column half, padded rows
-    // (read as float4: 16-byte aligned); in store launches four 32 x 16
-    // slices per half, one per epilogue warp, stage diagonal chunks
+    // transposed W update: a 16 x 128 chunk of v per epilogue group (column
+    // half), padded rows (read as float4: 16-byte aligned); in store launches
+    // four 32 x 16 slices per group, one per epilogue warp, stage diagonal chunks
     alignas(16) float tstage[2][CH * kTStageLd];
 };
 
@@ -817,7 +817,7 @@ __device__ __forceinline__ void named_bar(int id) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(128) : "memory");
 }
 
-// Named barrier of the 128 threads of a column half that also returns the AND
+// Named barrier of the 128 threads of an epilogue group that also returns the AND
 // of their predicates: the four warps take every loop exit together, so none
 // is left waiting at a barrier the others no longer reach.
 __device__ __forceinline__ bool named_bar_and(int id, bool pred) {
