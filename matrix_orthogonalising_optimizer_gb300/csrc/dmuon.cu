@@ -96,8 +96,8 @@ void bucket_buffers(Bucket& b, int32_t precision) {
             set(BUF_RF, m * ldm, ELEM_F32);
             for (int k : {BUF_RB, BUF_P, BUF_Q0, BUF_Q1, BUF_RP}) set(k, m * split_ld(m), ELEM_BF16);
         } else {
+            // fp32 FFMA engine (the fp32 mode)
             for (int k : {BUF_RF, BUF_P, BUF_Q0, BUF_Q1, BUF_RP}) set(k, m * ldm, ELEM_F32);
-            if (precision == DMUON_PREC_BF16) set(BUF_QB, m * ldm, ELEM_BF16);
         }
     } else {
         set(BUF_X1, m * ldn, xt);
@@ -834,7 +834,7 @@ int dmuon_bind_workspace(dmuon_handle_t h, void* dev_ptr, size_t bytes) {
             };
             if (b.route == DMUON_BUCKET_GRAM) {
                 const Operand X0 = buf(p, BUF_X0), RF = buf(p, BUF_RF), RB = buf(p, BUF_RB), P = buf(p, BUF_P),
-                              Q0 = buf(p, BUF_Q0), Q1 = buf(p, BUF_Q1), RP = buf(p, BUF_RP), QB = buf(p, BUF_QB);
+                              Q0 = buf(p, BUF_Q0), Q1 = buf(p, BUF_Q1), RP = buf(p, BUF_RP);
                 const Operand Rop = eng == kKernelTc ? RB : RF;
                 {  // R0 = inv^2 X X^T
                     GroupSpec s;
@@ -869,14 +869,12 @@ int dmuon_bind_workspace(dmuon_handle_t h, void* dev_ptr, size_t bytes) {
                     // P0 is also Q0: it is stored once, in Q0, where step 0's R P and
                     // R update read it
                     s.out[0] = first ? Q0 : P;
-                    if (first && QB.p) s.out[1] = QB;
                     split_outputs(s);
                     if ((rc = add(first ? G_POLY0 : G_POLY, s))) return rc;
                 }
                 for (int dir = 0; dir < 2; ++dir) {  // Q <- P Q
                     GroupSpec s = sym_spec(eng, P, dir == 0 ? Q0 : Q1);
                     s.out[0] = dir == 0 ? Q1 : Q0;
-                    if (QB.p) s.out[1] = QB;
                     split_outputs(s);
                     if ((rc = add(dir == 0 ? G_Q01 : G_Q10, s))) return rc;
                 }
@@ -901,7 +899,7 @@ int dmuon_bind_workspace(dmuon_handle_t h, void* dev_ptr, size_t bytes) {
                 for (int qb = 0; qb < 2; ++qb) {  // W update from inv * Q X
                     GroupSpec s;
                     s.kernel = bf16 ? kKernelTc : kKernelSimt;
-                    s.a = QB.p ? QB : (qb == 0 ? Q0 : Q1);
+                    s.a = qb == 0 ? Q0 : Q1;
                     s.b = X0;
                     s.b_mn = true;
                     s.M = m;

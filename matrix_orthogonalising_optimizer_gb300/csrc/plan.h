@@ -20,7 +20,6 @@ enum BufKind : int {
     BUF_Q0,
     BUF_Q1,
     BUF_RP,      // R P
-    BUF_QB,      // bf16 Q for the tensor-core final product (fp32 m x m engine)
     BUF_AB,      // operand A (direct, tensor cores)
     BUF_BB,      // B = bA + cA^2 (direct)
     BUF_PART,    // sum-of-squares partials

@@ -52,9 +52,7 @@ def per_matrix_bytes(m: int, n: int, precision: int, route: int, engine: int) ->
             # Rf; R, P, Q0, Q1, RP as bf16 rows [hi | lo], each part m rounded up to 64
             bufs += [m * ldm * 4] + [m * 2 * _up(m, 64) * 2] * 5
         else:
-            bufs += [m * ldm * 4] * 5                      # R, P, Q0, Q1, RP
-            if precision == PREC_BF16:
-                bufs += [m * ldm * 2]                      # bf16 Q for the final product
+            bufs += [m * ldm * 4] * 5                      # R, P, Q0, Q1, RP (fp32 mode)
     else:
         if precision == PREC_BF16:
             bufs += [m * ldn * 2, m * ldm * 2, m * ldm * 2]              # X1; A, B (bf16)
