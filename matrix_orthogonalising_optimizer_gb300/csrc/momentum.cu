@@ -88,6 +88,10 @@ __device__ __forceinline__ void unpack8(const uint4& q, float (&v)[8]) {
     }
 }
 
+__device__ __forceinline__ void prefetch_l2(uint64_t addr) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(addr));
+}
+
 // Registers are capped so five blocks fit on an SM with both rows' loads in
 // flight per thread.
 constexpr int kMomMinBlocks = 5;
@@ -135,6 +139,25 @@ __global__ void __launch_bounds__(kMomThreads, kMomMinBlocks) momentum_pack_kern
         const int r0 = (local / mi.tiles_c) * T, c0 = (local % mi.tiles_c) * T;
         const int rows = mi.rows, cols = mi.cols;
         const int dt = mi.dtype;
+        // L2 prefetch of this block's next tile in the same matrix (grad and
+        // momentum rows): its loads then wait on L2, not HBM.  Thread tid
+        // takes row tid / 4 of that tile; bit 1 picks the array, bit 0 the
+        // first or the last 128-byte line of the row's segment (the last one
+        // only where it is another line).
+        if (t + gridDim.x < end) {
+            const int l2 = static_cast<int>(t + gridDim.x - begin);
+            const int pr = (l2 / mi.tiles_c) * T + tid / 4, pc = (l2 % mi.tiles_c) * T;
+            if (pr < rows) {
+                const int es = dt == ELEM_BF16 ? 2 : 4;
+                const int64_t e0 = static_cast<int64_t>(pr) * cols + pc;
+                const int64_t e1 = static_cast<int64_t>(pr) * cols + min(pc + T, cols) - 1;
+                const char* arr = static_cast<const char*>((tid & 2) ? static_cast<const void*>(mom) : grad);
+                const uint64_t first = reinterpret_cast<uint64_t>(arr + e0 * es);
+                const uint64_t last = reinterpret_cast<uint64_t>(arr + e1 * es);
+                if (!(tid & 1)) prefetch_l2(first);
+                else if ((last >> 7) != (first >> 7)) prefetch_l2(last);
+            }
+        }
         // 128-bit access along rows needs every row start on 16 bytes
         const bool rows_vec = (static_cast<int64_t>(cols) * (dt == ELEM_BF16 ? 2 : 4)) % 16 == 0;
         float ss = 0.0f;
@@ -206,28 +229,29 @@ __global__ void __launch_bounds__(kMomThreads, kMomMinBlocks) momentum_pack_kern
 
         if (mi.transposed) {  // the same for the whole block
             __syncthreads();
-            // packed row = original column; 16 consecutive original rows per thread
-            const int xr = tid / 4, rr0 = (tid % 4) * 16;
+            // packed row = original column: a quad of threads per packed row,
+            // thread q taking original rows 8q .. 8q + 7 and 32 + 8q .. 32 + 8q + 7,
+            // so each store instruction covers whole sectors (rows 0 .. 31 of
+            // the segment, then 32 .. 63) and the shared-memory reads hit 32
+            // different banks
+            const int xr = tid / 4, q = tid % 4;
             const int c = c0 + xr;
             if (c < cols) {
-                float v[16];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) v[e] = tile[buf][rr0 + e][xr];
-                const int r = r0 + rr0;
-                const int64_t base = static_cast<int64_t>(c) * mi.ldx + r;
-                if (r + 16 <= rows) {
-                    float v0[8], v1[8];
+                for (int h = 0; h < 2; ++h) {
+                    const int rr0 = 8 * q + 32 * h;
+                    float v[8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        v0[e] = v[e];
-                        v1[e] = v[8 + e];
+                    for (int e = 0; e < 8; ++e) v[e] = tile[buf][rr0 + e][xr];
+                    const int r = r0 + rr0;
+                    const int64_t base = static_cast<int64_t>(c) * mi.ldx + r;
+                    if (r + 8 <= rows) {
+                        store8(mi.x, base, mi.x_type, v);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            if (r + e < rows) st1(mi.x, base + e, mi.x_type, v[e]);
                     }
-                    store8(mi.x, base, mi.x_type, v0);
-                    store8(mi.x, base + 8, mi.x_type, v1);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        if (r + e < rows) st1(mi.x, base + e, mi.x_type, v[e]);
                 }
             }
             buf ^= 1;

@@ -152,6 +152,29 @@ def test_momentum_many_one_tile_matrices():
     assert max(errs) <= TOL["bf16"], max(errs)
 
 
+def test_momentum_tall_transposes_ragged_and_interleaved():
+    # Tall matrices are transposed through shared memory, a quad of threads
+    # per packed row: rows whose 64-row segment ends inside a tile (1000 and
+    # 130 rows) are stored element-wise at their end, and rows of odd length
+    # (65, 41 columns) are not on 16 bytes.  About 4 000 tiles over the
+    # persistent blocks, each of which meets several kinds; the step is
+    # repeated to catch a race on the shared tile.
+    shapes = ([(1000, 136)] * 20 + [(1000, 130)] * 20 + [(130, 64)] * 60 + [(130, 65)] * 60
+              + [(72, 40)] * 40 + [(75, 41)] * 40)
+    inputs = make_inputs(shapes, "bf16", 23)
+    w1, m_new, _ = run_step(shapes, inputs, "bf16", lr=LR, beta=BETA, wd=WD)
+    w2, _, _ = run_step(shapes, inputs, "bf16", lr=LR, beta=BETA, wd=WD)
+    for i, (w, g, m) in enumerate(inputs):
+        want_m = oracle.round_to_storage(BETA * m.double().numpy() + g.double().numpy(), "bf16")
+        assert ulp_diff(m_new[i], torch.from_numpy(want_m).to(torch.bfloat16)).max() <= 1, (i, shapes[i])
+        assert torch.equal(w1[i], w2[i]), (i, shapes[i])
+    picks = [0, 19, 20, 39, 40, 99, 100, 159, 160, 199, 200, 239]
+    got, _ = gpu_O(shapes, inputs, "bf16", beta=BETA)
+    want = oracle_O([inputs[i] for i in picks], beta=BETA)
+    errs = [rel_fro(got[i], w) for i, w in zip(picks, want)]
+    assert max(errs) <= TOL["bf16"], max(errs)
+
+
 @pytest.mark.gpu
 def test_flat_momentum_pass():
     # A wave whose wide bf16 matrices of at least 2^20 elements hold 2^26 or
