@@ -475,26 +475,33 @@ def measure_config(name, steps, warmup, peaks, src, cpu, oracle_rate=None):
     for _ in range(warmup):
         muon.step(ws, gs, ms, lr, beta, wd, T, stream)
     torch.cuda.synchronize()
-    muon.set_timing(True)
-    per_step = []
-    if flush:
-        for _ in range(steps):
-            scrub.zero_()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            muon.step(ws, gs, ms, lr, beta, wd, T, stream)
-            e1.record(stream)
-            per_step.append((e0, e1))
-        torch.cuda.synchronize()
-        ms_step = sum(a.elapsed_time(b) for a, b in per_step) / steps
-    else:
+
+    def timed_steps():
+        per_step = []
+        if flush:
+            for _ in range(steps):
+                scrub.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                muon.step(ws, gs, ms, lr, beta, wd, T, stream)
+                e1.record(stream)
+                per_step.append((e0, e1))
+            torch.cuda.synchronize()
+            return sum(a.elapsed_time(b) for a, b in per_step) / steps
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(steps):
             muon.step(ws, gs, ms, lr, beta, wd, T, stream)
         e1.record(stream)
         torch.cuda.synchronize()
-        ms_step = e0.elapsed_time(e1) / steps
+        return e0.elapsed_time(e1) / steps
+
+    # the step time without the stage timers (whose events between launches
+    # keep each launch from starting while the previous one finishes), then
+    # the same steps again with them for the stage split and the GEMM rate
+    ms_step = timed_steps()
+    muon.set_timing(True)
+    ms_with_timers = timed_steps()
     timing = muon.timing()
     muon.set_timing(False)
     status = muon.device_status(stream)
@@ -508,6 +515,7 @@ def measure_config(name, steps, warmup, peaks, src, cpu, oracle_rate=None):
     tc_ms = timing["tc"][0] / steps
     out = {"workload": workloads_name(cfg), "matrices": len(cfg.shapes), "steps": steps, "warmup": warmup,
            "ms_per_step": ms_step, "matrices_per_s": len(cfg.shapes) / (ms_step / 1000.0),
+           "ms_per_step_with_stage_timers": ms_with_timers,
            "dtype": "bf16" if cfg.precision == "bf16" else "fp32",
            "l2": "L2 flushed (512 MB write) before every timed step" if flush
            else "inputs larger than L2 (resident in HBM)",

@@ -926,6 +926,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     const uint32_t tmem = S.tmem_base;
     const int rank = static_cast<int>(cluster_rank());
     const int total = L.total_tiles;
+    // The launch may start while the previous kernel in the stream finishes
+    // (programmatic dependent launch): the set-up above touches only this
+    // CTA's shared memory and TMEM; global memory waits for that kernel's
+    // completion and its writes.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     // Register split, warpgroup-uniform; each role's code sits inside the
     // branch of its own setmaxnreg, so it is compiled to that budget.
@@ -963,7 +968,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
                 t = wait_tile(S.tile_full, S.tile_slot, k, L.status, total);
                 release_tile(S.tile_empty, k);
             }
-            if (t >= total) break;
+            if (t >= total) {
+                // no tile left to claim: the next launch's CTAs may be placed
+                // on SMs as this launch's CTAs leave them
+                asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+                break;
+            }
             const TileCoord tc = decode_tile(L, t);
             const GemmGroup* g = L.groups + L.idx[tc.gi];
             const int nkb = (g->K + SLAB_K - 1) / SLAB_K;
@@ -1220,16 +1230,20 @@ cudaError_t launch_gemm_tc(const LaunchList& l, int num_sms, cudaStream_t s) {
     static PerDevice max_pairs_per_device;
     const size_t smem = gemm_tc_smem_bytes();
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = kPair;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // programmatic dependent launch: the kernel waits (griddepcontrol.wait)
+    // for the previous kernel before its first global-memory access
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.blockDim = dim3(kTcThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -1245,6 +1259,7 @@ cudaError_t launch_gemm_tc(const LaunchList& l, int num_sms, cudaStream_t s) {
         if (r != cudaSuccess) return r;
         cudaLaunchConfig_t probe = cfg;
         probe.gridDim = dim3(num_sms / kPair * kPair);
+        probe.numAttrs = 1;  // the cluster shape alone
         int n = 0;
         r = cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<false>, &probe);
         if (r != cudaSuccess) return r;
