@@ -939,8 +939,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------ TMA producer
         uint32_t stage = 0, phase = 0;
-        uint32_t issued = 0, issued_parity = 0;  // per-stage bit masks
+        uint32_t n_issued = 0;  // slabs issued so far (ring position n_issued % STAGES)
         bool ok = true;
+        const uint32_t full0 = mapa(saddr(&S.full[0]), 0);  // the leader's barriers, 8 bytes apart
         for (int j = 0; j < L.n; ++j) {
             tensormap_acquire(&L.groups[L.idx[j]].tma_a);
             tensormap_acquire(&L.groups[L.idx[j]].tma_b);
@@ -989,24 +990,27 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
             const int zb = pk > 1 ? tc.mat + rank * (pk >> 1) : tc.mat;
             const CUtensorMap* map_a = &g->tma_a;
             const CUtensorMap* map_b = &g->tma_b;
+            // K segment of the slab and its offset inside it (split operands:
+            // segment t reads A's part t % 2 and B's part t / 2), advanced
+            // without a division
+            int seg = 0, within = 0;
             for (int kb = 0; kb < nkb; ++kb) {
                 if (!mbar_wait(&S.empty[stage], phase ^ 1, L.status)) {
                     ok = false;
                     break;
                 }
                 if (rank == 0) mbar_expect_tx(&S.full[stage], STAGE_TX);
-                issued |= 1u << stage;
-                issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                ++n_issued;
                 // own 128 rows of A and own 128 columns of B, counted on the
                 // leader's barrier
-                const uint32_t fb = mapa(saddr(&S.full[stage]), 0);
-                // K coordinates of this slab in A and in B (split operands:
-                // segment t of K reads A's segment t % 2, B's t / 2)
-                int ka = kb * SLAB_K, kbk = ka;
-                if (kseg > 0) {
-                    const int seg = ka / kseg, within = ka - seg * kseg;
-                    ka = (seg & 1) * kseg + within;
-                    kbk = (seg >> 1) * kseg + within;
+                const uint32_t fb = full0 + stage * static_cast<uint32_t>(sizeof(uint64_t));
+                // K coordinates of this slab in A and in B (no split: kseg = 0,
+                // seg stays 0)
+                const int ka = (seg & 1) * kseg + within, kbk = (seg >> 1) * kseg + within;
+                within += SLAB_K;
+                if (within == kseg) {
+                    within = 0;
+                    ++seg;
                 }
                 tma_load_3d_pair(S.a[stage], map_a, fb, ka, a_row, zb);
                 if (!b_mn) {
@@ -1027,8 +1031,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
             // leader's barrier counts both CTAs' copies; the partner waits
             // for the leader at the final cluster barrier)
             if (rank == 0)
-                for (int s = 0; s < STAGES; ++s)
-                    if (issued & (1u << s)) mbar_wait(&S.full[s], (issued_parity >> s) & 1u, L.status);
+                for (uint32_t j = 1; j <= STAGES && j <= n_issued; ++j) {
+                    const uint32_t q = n_issued - j;  // a slab issued last, at ring slot q % STAGES
+                    mbar_wait(&S.full[q % STAGES], (q / STAGES) & 1u, L.status);
+                }
         } else {
             // wait for the MMA's releases of the last ring round, so no
             // commit from the leader is still in flight towards this CTA

@@ -247,6 +247,14 @@ def test_symmetric_operands_bitwise():
     _, _, m32 = run_step(shapes, inputs, "bf16", lr=LR, beta=BETA, wd=WD, precision="fp32")
     assert {b["engine"] for b in m32.buckets()} == {1}
     _check_symmetric_operands(m32, m32.workspace, m32.buckets())
+    # split operands over several 256-row pair tiles (small_m raised): hi and
+    # lo parts mirrored across tiles; O to the oracle
+    big = [(520, 1600), (1600, 520), (300, 1000)]
+    big_in = make_inputs(big, "bf16", 24)
+    _, _, ms = run_step(big, big_in, "bf16", lr=LR, beta=BETA, wd=WD, small_m=1024)
+    assert {b["engine"] for b in ms.buckets()} == {2}
+    _check_symmetric_operands(ms, ms.workspace, ms.buckets())
+    check_O(big, big_in, "bf16", small_m=1024)
 
 
 def _check_symmetric_operands(muon, ws, buckets):
