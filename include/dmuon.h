@@ -39,7 +39,11 @@
  *    previous step uploads the new pointer table with one pageable copy.
  *    With the same pointer set as the previous call it issues only stream
  *    work (memsets and kernel launches), so such a call can be captured in a
- *    CUDA graph and replayed (timers off).
+ *    CUDA graph and replayed (timers off).  The tensor-core launches after
+ *    the step's first kernel are programmatic dependent launches: each may be
+ *    placed while the one before it finishes and touches global memory only
+ *    after that one has completed; the step's first kernel waits for the
+ *    caller's earlier work in the ordinary way.
  *  - Errors are negative status codes; dmuon_last_error() gives the message
  *    of the calling thread's last failure.  A handle must not be used on two
  *    streams at once.
