@@ -48,6 +48,8 @@
 // the epilogue warps' arrivals on them are relaxed (see their call sites).
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "epilogue.cuh"
 
 namespace dmuon {
@@ -554,6 +556,7 @@ __device__ __forceinline__ void epi_prefetch(const EpiRegs& e, int r, int r0, in
 }
 
 // Prefetched input of a chunk: W for the update, else the aux operand.
+template <bool kUpd>
 __device__ __forceinline__ void epi_load(const EpiRegs& e, int r, int r0, int lane, int c0, float (&x)[CH]) {
     if (r0 >= e.M || c0 >= e.N) return;  // warp-uniform
     const int ncol = min(CH, e.N - c0);
@@ -562,7 +565,7 @@ __device__ __forceinline__ void epi_load(const EpiRegs& e, int r, int r0, int la
     int32_t type, ld;
     bool by_col;
     bool vec;
-    if (e.update()) {
+    if (kUpd) {
         base = e.w;
         type = e.w_type();
         ld = e.w_cols;
@@ -706,14 +709,14 @@ __device__ __forceinline__ void epi_store_diag(const EpiRegs& e, int r0, int lan
 // W (in place of the loaded W values), to keep the register footprint low.
 // kSplit: the launch holds groups with split outputs (the other instance
 // carries none of their code).
-template <bool kSplit>
+template <bool kSplit, bool kUpd>
 __device__ __forceinline__ void epi_finish(const EpiRegs& e, int r, int r0, int lane, int c0, float (&v)[CH],
                                            float (&x)[CH], float* stg) {
     if (r0 >= e.M) return;  // warp-uniform: no row of this warp exists
     const bool valid = r < e.M;
     const int ncol = min(CH, e.N - c0);
     const bool full = ncol == CH;
-    const bool upd = e.update();
+    constexpr bool upd = kUpd;
     if (upd && e.aux) {
         // the update that also has an aux term (direct route: a X + B X) reads
         // the aux chunk here; x already holds W
@@ -1184,24 +1187,31 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
             // transposed-update stage: a launch holds store groups or update
             // groups, never both)
             float* stg = S.tstage[half] + q * (32 * CH);
-            float xin[CH];
-            if (nch > 0) epi_load(e, r, r0w, lane, cbase, xin);
-            // a wait that gave up skips the tile's work but not the loop: the
-            // group then leaves together at the next tile slot (the producer
-            // stops publishing once its own waits give up)
-            const bool ready = mbar_wait_cluster(&S.acc_full[buf], use & 1, L.status);
-            tc_fence_after();
-            for (int kc = 0; ready && kc < nch; ++kc) {
-                const int c0 = cbase + kc * CH;
-                float x[CH];
+            // the chunk loop compiled per kind: stores, or the W update
+            auto chunks = [&](auto upd_c) {
+                constexpr bool kUpd = decltype(upd_c)::value;
+                float xin[CH];
+                if (nch > 0) epi_load<kUpd>(e, r, r0w, lane, cbase, xin);
+                // a wait that gave up skips the tile's work but not the loop: the
+                // group then leaves together at the next tile slot (the producer
+                // stops publishing once its own waits give up)
+                const bool ready = mbar_wait_cluster(&S.acc_full[buf], use & 1, L.status);
+                tc_fence_after();
+                for (int kc = 0; ready && kc < nch; ++kc) {
+                    const int c0 = cbase + kc * CH;
+                    float x[CH];
 #pragma unroll
-                for (int j = 0; j < CH; ++j) x[j] = xin[j];
-                if (kc + 1 < nch) epi_load(e, r, r0w, lane, c0 + CH, xin);
-                float v[CH];
-                __syncwarp();
-                tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN + tcol0 + kc * CH), v);
-                epi_finish<kSplit>(e, r, r0w, lane, c0, v, x, stg);
-            }
+                    for (int j = 0; j < CH; ++j) x[j] = xin[j];
+                    if (kc + 1 < nch) epi_load<kUpd>(e, r, r0w, lane, c0 + CH, xin);
+                    float v[CH];
+                    __syncwarp();
+                    tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) +
+                                  static_cast<uint32_t>(buf * BN + tcol0 + kc * CH), v);
+                    epi_finish<kSplit, kUpd>(e, r, r0w, lane, c0, v, x, stg);
+                }
+            };
+            if (e.update()) chunks(std::true_type{});
+            else chunks(std::false_type{});
             }
             // Release the accumulator.  Each tcgen05.ld of it ended with
             // tcgen05.wait::ld before its values were used, so every read of
