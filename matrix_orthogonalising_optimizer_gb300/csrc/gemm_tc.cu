@@ -891,7 +891,7 @@ __device__ __forceinline__ void tw_store(const EpiRegs& e, int c0, int q, int wc
     }
 }
 
-template <bool kSplit>
+template <bool kSplit, bool kUpd>
 __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_constant__ LaunchList L) {
     extern __shared__ uint8_t smem_raw[];
     Smem& S = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -1155,7 +1155,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
             if (nch > 0) epi_prefetch(e, r, r0w, lane, cbase, nch * CH);
             // tall matrices' update through the staged path (the same four warps
             // of this half always see the same nch, so the named barriers match)
-            const bool tpath = e.update() && e.transposed() && !e.aux && (e.w_cols % 4) == 0;
+            const bool tpath = kUpd && e.transposed() && !e.aux && (e.w_cols % 4) == 0;
             if (tpath) {
                 const int wc = tm * BM + 4 * lane;
                 float* stg = S.tstage[half];
@@ -1210,8 +1210,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
                     epi_finish<kSplit, kUpd>(e, r, r0w, lane, c0, v, x, stg);
                 }
             };
-            if (e.update()) chunks(std::true_type{});
-            else chunks(std::false_type{});
+            chunks(std::integral_constant<bool, kUpd>{});
             }
             // Release the accumulator.  Each tcgen05.ld of it ended with
             // tcgen05.wait::ld before its values were used, so every read of
@@ -1267,17 +1266,20 @@ cudaError_t launch_gemm_tc(const LaunchList& l, int num_sms, cudaStream_t s) {
     // pairs counted, once per device with that device current
     int max_pairs = 0;
     e = max_pairs_per_device.get(dev, &max_pairs, [&](int* out) {
-        cudaError_t r = cudaFuncSetAttribute(gemm_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
+        cudaError_t r = cudaFuncSetAttribute(gemm_tc_kernel<false, false>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (r == cudaSuccess)
-            r = cudaFuncSetAttribute(gemm_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            r = cudaFuncSetAttribute(gemm_tc_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(smem));
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(gemm_tc_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      static_cast<int>(smem));
         if (r != cudaSuccess) return r;
         cudaLaunchConfig_t probe = cfg;
         probe.gridDim = dim3(num_sms / kPair * kPair);
         probe.numAttrs = 1;  // the cluster shape alone
         int n = 0;
-        r = cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<false>, &probe);
+        r = cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<false, false>, &probe);
         if (r != cudaSuccess) return r;
         *out = n > 0 ? n : num_sms / kPair;
         return cudaSuccess;
@@ -1292,8 +1294,14 @@ cudaError_t launch_gemm_tc(const LaunchList& l, int num_sms, cudaStream_t s) {
     // its update launch and 2 % on sets of ~4 tiles per pair.
     LaunchList run = l;
     run.epi_sets = (!l.update && l.total_tiles >= 8 * pairs) ? 1 : 0;
-    if (l.has_split) return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<true>, run);
-    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<false>, run);
+    // three instances: store launches with and without split outputs, update
+    // launches (which store nothing, so never split outputs)
+    if (l.update) {
+        if (l.has_split) return cudaErrorInvalidValue;
+        return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<false, true>, run);
+    }
+    if (l.has_split) return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<true, false>, run);
+    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<false, false>, run);
 }
 
 }  // namespace dmuon
