@@ -1116,8 +1116,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
             const int t = wait_tile_acquire(S.tile_full, S.tile_slot, k, L.status, total);
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster_relaxed(mapa(saddr(&S.tile_empty[k % kTileRing]), 0));
-            // the group leaves together (a wait that gave up counts for all four)
-            if (!named_bar_and(1 + half, t < total)) break;
+            // The group leaves together (a wait that gave up counts for all
+            // four): update launches' staged path has group barriers.  Store
+            // launches have none, so with column halves each warp leaves on
+            // its own; with sets the barrier also parks the warps of the set
+            // that skips this tile (measured: faster than letting them run on)
+            if (kUpd || sets) {
+                if (!named_bar_and(1 + half, t < total)) break;
+            } else if (t >= total) {
+                break;
+            }
             if (sets && (k & 1) != half) continue;
             const TileCoord tc = decode_tile(L, t);
             const GemmGroup& g = L.groups[L.idx[tc.gi]];
